@@ -1,0 +1,61 @@
+"""Sets a synthetic workload up in a GPU pool (harness for tests and bench.py).
+
+Plumbing only: page mapping, hot-buffer leases and row contents come from
+``workloads``; every operation goes through the C ABI binding.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import tiered_sparse_mla_gb300 as hs
+import workloads as W
+
+
+class GpuWorkload:
+    """A workload's pool, its request tables and the step buffers on cuda:0."""
+
+    def __init__(self, w: W.Workload, stream=None, build_topk: bool = True):
+        self.w = w
+        lay = self.lay = W.layout(w)
+        has_host = bool((lay.page_host >= 0).any())
+        dtype = hs.HS_BF16 if w.dtype == "bf16" else hs.HS_FP8_E4M3_ROWSCALE
+        self.pool = hs.Pool(dtype=dtype, n_gpu_blocks=lay.n_gpu_blocks,
+                            n_host_blocks=lay.n_host_blocks if has_host else 0,
+                            max_requests=w.B, max_ctx=w.ctx, max_topk=w.K,
+                            hot_rows=w.hot_rows, stream=stream)
+        for r in range(w.B):
+            self.pool.request_init(r, w.ctx)
+            self.pool.page_map_range(r, 0, lay.page_gpu[r], lay.page_host[r])
+            self.pool.hot_lease(r, lay.hot_blocks[r])
+        W.fill_rows(w.dtype, self.pool.gpu_rows(), self.pool.gpu_scales(), W.row_seed(w, "gpu"))
+        if has_host:
+            hr = torch.from_numpy(self.pool.host_rows())
+            hsc = self.pool.host_scales()
+            W.fill_rows(w.dtype, hr, None if hsc is None else torch.from_numpy(hsc),
+                        W.row_seed(w, "host"), gen_device="cuda")
+        torch.cuda.synchronize()
+        dev = "cuda"
+        B, K, rb = w.B, w.K, w.row_bytes
+        self.req_ids = torch.arange(B, dtype=torch.int32, device=dev)
+        self.resolved = torch.empty((B, K), dtype=torch.int32, device=dev)
+        self.gathered = torch.empty((B, K, rb), dtype=torch.uint8, device=dev)
+        self.gscale = torch.empty((B, K), dtype=torch.float32, device=dev) if w.dtype == "fp8" else None
+        self.counts = torch.empty((B, 3), dtype=torch.int32, device=dev)
+        self.out = torch.empty((B, w.T, w.H, 512), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((B, w.T, w.H), dtype=torch.float32, device=dev)
+        ws = hs.hs_decode_workspace_bytes(B, w.T, w.H, K)
+        self.workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
+        self.topk_host = np.stack(list(W.topk_lists(w))) if build_topk else None
+        self.topk = torch.from_numpy(self.topk_host).to(dev) if build_topk else None
+
+    def resolve(self, step: int, topk=None, stream=None):
+        t = self.topk[step] if topk is None else topk
+        self.pool.resolve_topk(self.req_ids, t, self.resolved, self.gathered, self.gscale,
+                               self.counts, stream)
+
+    def decode(self, step: int, q, topk=None, stream=None):
+        t = self.topk[step] if topk is None else topk
+        self.pool.sparse_mla_decode(q, self.gathered, self.gscale, self.resolved, t,
+                                    self.req_ids, self.w.sm_scale, self.out, self.lse,
+                                    self.workspace, stream)

@@ -1,0 +1,155 @@
+"""GPU parity of the fused resolve kernel against the oracle (bit-exact).
+
+Same seeded inputs on both sides; per step every resolved row id, every
+gathered byte and scale, the (resident, hot, miss) counts, the device error
+bits and the whole hot-buffer state (slot_tag, slot_stamp, pos_to_slot, clock)
+must be identical. The GPU's extra LRU order must equal argsort(stamp, slot).
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__ as g
+    g.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+def _run(w, steps=None, nthreads=4, topk_override=None):
+    from harness import GpuWorkload
+    from _mirror import compare_resolve, oracle_mirror
+    gw = GpuWorkload(w)
+    ot = oracle_mirror(gw)
+    lists = gw.topk_host if topk_override is None else topk_override
+    n = len(lists) if steps is None else min(steps, len(lists))
+    tot = np.zeros(3, np.int64)
+    for s in range(n):
+        t = torch.from_numpy(np.ascontiguousarray(lists[s])).cuda()
+        gw.resolve(s, topk=t)
+        err = gw.pool.get_error()
+        out = ot.resolve(np.arange(w.B), lists[s], nthreads=nthreads)
+        compare_resolve(gw, ot, *out, err, s)
+        tot += out[3].sum(axis=0)
+    gw.pool.close()
+    return tot
+
+
+SMALL = {
+    "tiny": W.WORKLOADS["tiny"],
+    "resident": W.WORKLOADS["resident"].scaled(B=3, ctx=16384, steps=3),
+    "hybrid": W.WORKLOADS["hybrid"].scaled(B=3, ctx=65536, resident_tail=8192, steps=8),
+    "hybrid_ragged": W.WORKLOADS["hybrid"].scaled(B=2, ctx=32768, resident_tail=4096, K=1000,
+                                                   hot_rows=2048, tail=100, steps=6),
+    "noresident": W.WORKLOADS["noresident"].scaled(B=4, ctx=65536, steps=5),
+    "noresident_small_k": W.WORKLOADS["noresident"].scaled(B=5, ctx=4096, K=37, hot_rows=128,
+                                                            steps=7),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_resolve_parity_small(name):
+    tot = _run(SMALL[name])
+    assert tot.sum() > 0
+
+
+@pytest.mark.parametrize("name,steps", [("resident", 2), ("hybrid", 3), ("noresident", 2)])
+def test_resolve_parity_full_size(name, steps):
+    """The full-size workloads, first steps, every request compared."""
+    tot = _run(W.WORKLOADS[name], steps=steps, nthreads=16)
+    assert tot.sum() == W.WORKLOADS[name].B * W.WORKLOADS[name].K * steps
+
+
+def test_resolve_error_paths():
+    """Out-of-range, repeated and host-less positions, padding and a bad request id:
+    the same -1 entries, counts and error bits as the oracle."""
+    w = W.WORKLOADS["tiny"].scaled(B=3, steps=2)
+    lay = W.layout(w)
+    rng = np.random.default_rng(3)
+    lists = np.stack(list(W.topk_lists(w)))
+    bad = lists.copy()
+    bad[0, 0, :5] = [-1, -7, w.ctx, w.ctx + 100, -1]
+    bad[0, 1, 10:14] = [3, 3, 3, 5]            # position 3 misses three times
+    bad[1, 2, 20:22] = [9, 9]
+    from harness import GpuWorkload
+    from _mirror import compare_resolve, oracle_mirror
+    gw = GpuWorkload(w)
+    # request 2, page 1: neither resident nor copied to host
+    gw.pool.page_map(2, 1, -1, -1)
+    ot = oracle_mirror(gw)
+    ot.page_host[2, 1] = -1
+    bad[0, 2, 30:33] = [64, 65, 127]
+    for s in range(2):
+        t = torch.from_numpy(bad[s]).cuda()
+        gw.resolve(s, topk=t)
+        err = gw.pool.get_error()
+        out = ot.resolve(np.arange(w.B), bad[s])
+        assert out[4] != 0
+        compare_resolve(gw, ot, *out, err, s)
+    # a request id outside the pool
+    rid = torch.tensor([0, 7, 2], dtype=torch.int32, device="cuda")
+    gw.pool.resolve_topk(rid, torch.from_numpy(lists[1]).cuda(), gw.resolved, gw.gathered,
+                         gw.gscale, gw.counts)
+    err = gw.pool.get_error()
+    assert err & 8
+    assert (gw.resolved[1] == -1).all() and (gw.counts[1] == 0).all()
+    assert not gw.gathered[1].any()
+    gw.pool.close()
+
+
+def test_host_side_argument_errors():
+    import tiered_sparse_mla_gb300 as hs
+    w = W.WORKLOADS["tiny"]
+    from harness import GpuWorkload
+    gw = GpuWorkload(w, build_topk=False)
+    big = torch.zeros((1, w.hot_rows + 64), dtype=torch.int32, device="cuda")
+    res = torch.empty_like(big)
+    gat = torch.empty((1, big.shape[1], w.row_bytes), dtype=torch.uint8, device="cuda")
+    cnt = torch.empty((1, 3), dtype=torch.int32, device="cuda")
+    with pytest.raises(hs.HsError) as e:
+        gw.pool.resolve_topk(gw.req_ids, big, res, gat, None, cnt)
+    assert e.value.status == hs.HS_ERR_CAPACITY
+    lib = hs.load()
+    t = torch.zeros((1, 8), dtype=torch.int32, device="cuda")
+    st = lib.hs_resolve_topk(gw.pool.handle, 1, None, t.data_ptr(), 8, t.data_ptr(),
+                             gat.data_ptr(), None, cnt.data_ptr(), None)
+    assert st == hs.HS_ERR_INVALID_ARG
+    st = lib.hs_resolve_topk(gw.pool.handle, 1, gw.req_ids.data_ptr(), t.data_ptr(), 8,
+                             t.data_ptr(), gat.data_ptr() + 4, None, cnt.data_ptr(), None)
+    assert st == hs.HS_ERR_INVALID_ARG
+    # FP8 scale pointer given to a BF16 pool
+    st = lib.hs_resolve_topk(gw.pool.handle, 1, gw.req_ids.data_ptr(), t.data_ptr(), 8,
+                             t.data_ptr(), gat.data_ptr(), t.data_ptr(), cnt.data_ptr(), None)
+    assert st == hs.HS_ERR_INVALID_ARG
+    with pytest.raises(hs.HsError):
+        gw.pool.page_map(0, 0, gw.pool.cfg.n_gpu_blocks, -1)
+    with pytest.raises(hs.HsError):
+        gw.pool.hot_lease(0, [0] * 3)
+    assert gw.pool.get_error() == 0
+    gw.pool.close()
+
+
+def test_snapshot_restore_replays_identically():
+    w = SMALL["hybrid"]
+    from harness import GpuWorkload
+    from _mirror import gpu_state
+    gw = GpuWorkload(w)
+    gw.resolve(0)
+    snap = gw.pool.snapshot()
+    outs = []
+    for rep in range(2):
+        if rep:
+            gw.pool.restore(snap)
+        for s in (1, 2, 3):
+            gw.resolve(s)
+        torch.cuda.synchronize()
+        outs.append((gw.resolved.cpu().clone(), gw.gathered.cpu().clone(), gpu_state(gw)))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    for k in outs[0][2]:
+        assert np.array_equal(outs[0][2][k], outs[1][2][k])
+    gw.pool.close()

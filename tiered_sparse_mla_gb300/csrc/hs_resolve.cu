@@ -1,0 +1,451 @@
+// hs_resolve.cu -- the fused top-K resolve kernel.
+//
+// One launch resolves a decode step's top-K lists against the tiered cache
+// ("vLLM GLM 5.3 优化：混合 HiSparse 卸载", section 混合 HiSparse 的技术实现, item 2;
+// "vLLM Hybrid HiSparse：稀疏MLA破解长上下文显存瓶颈", section 融合内核与CUDA图兼容):
+// a row in a resident page is read in place, a row in the request's hot buffer
+// is read and its LRU entry refreshed, and a missing row is copied by itself
+// from pinned host memory into the least recently used hot slot. The launch
+// shape depends only on (B, K), so the kernel replays inside a CUDA graph; the
+// LRU clock lives in device memory and advances on every replay.
+//
+// Orders the pages leave open (same readings as the oracle): hits are stamped
+// before any miss is placed; misses in ascending position take the unprotected
+// slots (stamp < clock) with the smallest (stamp, slot) keys; residency is
+// checked before the hot buffer; a missing position repeated in one list is
+// served once (first in list order).
+//
+// Design (GB300): one thread-block cluster of G CTAs per request.
+//   phase 1  every CTA classifies its K/G entries (page table, then
+//            pos_to_slot), stamps its hot hits and lists its misses in shared
+//            memory;                                    -> cluster barrier A
+//   rank 0   merges all CTAs' miss lists over distributed shared memory, sorts
+//            them (bitonic, in shared memory), picks victims from the
+//            persistent per-request LRU order (slots kept sorted by
+//            (stamp, slot), so the i-th unprotected entry is the i-th victim),
+//            updates tag / stamp / pos_to_slot / LRU order and writes each
+//            miss's slot back into its owner CTA's shared memory;
+//   others   meanwhile copy their resident and hot rows (16-byte vectors,
+//            several loads in flight per thread);       -> cluster barrier B
+//   phase 3  every CTA copies its miss rows from the device-mapped pinned host
+//            arena into the slot and into the gathered buffer.
+// Barriers are hardware cluster barriers: no spin loops.
+#include <cstdint>
+
+#include "hs_internal.cuh"
+
+namespace {
+
+constexpr int NT = 512;       // threads per CTA
+constexpr int UNROLL = 4;     // 16-byte vectors in flight per thread and round
+constexpr int KIND_NONE = 0, KIND_RES = 1, KIND_HOT = 2, KIND_MISS = 3;
+
+// Dynamic shared memory layout (bytes), identical in every CTA.
+struct Smem {
+    int chunk, kpad, K;
+    __host__ __device__ size_t off_src() const { return 0; }
+    __host__ __device__ size_t off_hrow() const { return off_src() + 4 * (size_t)chunk; }
+    __host__ __device__ size_t off_kind() const { return off_hrow() + 4 * (size_t)chunk; }
+    __host__ __device__ size_t off_mj() const { return off_kind() + 4 * (size_t)chunk; }
+    __host__ __device__ size_t off_mp() const { return off_mj() + 4 * (size_t)chunk; }
+    __host__ __device__ size_t off_misc() const { return off_mp() + 4 * (size_t)chunk; }
+    // misc: [0] local misses, [1] local resident, [2] local hot, [3..3+16) offsets,
+    //       [20..20+32) warp scan scratch
+    __host__ __device__ size_t off_keys() const { return (off_misc() + 4 * 64 + 15) & ~size_t(15); }
+    __host__ __device__ size_t off_rank() const { return off_keys() + 8 * (size_t)kpad; }
+    __host__ __device__ size_t off_victim() const { return off_rank() + 4 * (size_t)K; }
+    __host__ __device__ size_t total() const { return off_victim() + 4 * (size_t)K; }
+};
+
+__host__ __device__ inline int next_pow2(int x) {
+    int p = 1;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+template <int RB>
+__global__ void __launch_bounds__(NT, 2)
+resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
+               const int32_t *__restrict__ topk, int K, int chunk, int G,
+               int32_t *__restrict__ resolved, uint8_t *__restrict__ gathered,
+               float *__restrict__ gscale, int32_t *__restrict__ counts) {
+    constexpr int V = RB / 16;  // 16-byte vectors per row
+    extern __shared__ __align__(16) unsigned char smem[];
+    const Smem L{chunk, next_pow2(K), K};
+    int32_t *s_src = reinterpret_cast<int32_t *>(smem + L.off_src());
+    int32_t *s_hrow = reinterpret_cast<int32_t *>(smem + L.off_hrow());
+    int32_t *s_kind = reinterpret_cast<int32_t *>(smem + L.off_kind());
+    int32_t *s_mj = reinterpret_cast<int32_t *>(smem + L.off_mj());
+    int32_t *s_mp = reinterpret_cast<int32_t *>(smem + L.off_mp());
+    int32_t *s_misc = reinterpret_cast<int32_t *>(smem + L.off_misc());
+    int32_t *s_warp = s_misc + 20;
+    unsigned long long *s_keys = reinterpret_cast<unsigned long long *>(smem + L.off_keys());
+    int32_t *s_rank = reinterpret_cast<int32_t *>(smem + L.off_rank());
+    int32_t *s_victim = reinterpret_cast<int32_t *>(smem + L.off_victim());
+
+    const int tid = threadIdx.x;
+    const int g = static_cast<int>(hs::cluster_ctarank());
+    const int bi = blockIdx.y;
+    const int r = req_ids[bi];
+    const int j0 = g * chunk;
+    const int nloc = max(0, min(K, j0 + chunk) - j0);
+    const size_t row0 = (size_t)bi * K + j0;  // first gathered row of this CTA
+    const bool fp8 = gscale != nullptr;
+
+    if (r < 0 || r >= P.max_req) {
+        // the whole cluster takes this branch (same request), so no barrier waits
+        for (int l = tid; l < nloc; l += NT) {
+            resolved[row0 + l] = -1;
+            if (fp8) gscale[row0 + l] = 0.f;
+        }
+        for (int i = tid; i < nloc * V; i += NT)
+            hs::st_v4(gathered + row0 * RB + (size_t)i * 16, make_uint4(0, 0, 0, 0));
+        if (g == 0 && tid < 3) counts[bi * 3 + tid] = 0;
+        if (g == 0 && tid == 0) atomicOr(P.err, HS_DEVERR_BAD_REQUEST);
+        return;
+    }
+
+    const int C = P.C;
+    const int c = P.clock[r] + 1;  // this step's clock (rank 0 stores it after barrier A)
+    const int Lr = P.ctx[r];
+    const int2 *page = P.page + (size_t)r * P.max_pages;
+    const int32_t *hblk = P.hot_blocks + (size_t)r * P.HB;
+    int32_t *tag = P.tag + (size_t)r * C;
+    int32_t *stamp = P.stamp + (size_t)r * C;
+    int32_t *lru = P.lru + (size_t)r * C;
+    int32_t *p2s = P.p2s + (size_t)r * P.max_ctx;
+
+    if (tid == 0) s_misc[0] = s_misc[1] = s_misc[2] = 0;
+    __syncthreads();
+
+    // ---------------------------------------------------------------- phase 1
+    uint32_t err = 0;
+    int n_res = 0, n_hot = 0;
+    for (int l = tid; l < nloc; l += NT) {
+        const int p = topk[row0 + l];
+        int kind = KIND_NONE, src = -1, hrow = -1;
+        if (p == -1) {
+        } else if (p < 0 || p >= Lr || p >= P.max_ctx) {
+            err |= HS_DEVERR_INDEX_RANGE;
+        } else {
+            const int2 e = page[p >> 6];
+            if (e.x >= 0) {
+                kind = KIND_RES;
+                src = e.x * hs::kPage + (p & 63);
+                ++n_res;
+            } else {
+                const int s = p2s[p];
+                if (s >= 0) {
+                    kind = KIND_HOT;
+                    src = hblk[s >> 6] * hs::kPage + (s & 63);
+                    stamp[s] = c;
+                    ++n_hot;
+                } else if (e.y < 0) {
+                    err |= HS_DEVERR_NO_HOST;
+                } else {
+                    kind = KIND_MISS;
+                    hrow = e.y * hs::kPage + (p & 63);
+                    const int m = atomicAdd(&s_misc[0], 1);
+                    s_mj[m] = l;
+                    s_mp[m] = p;
+                }
+            }
+        }
+        s_kind[l] = kind;
+        s_src[l] = src;
+        s_hrow[l] = hrow;
+    }
+    if (n_res) atomicAdd(&s_misc[1], n_res);
+    if (n_hot) atomicAdd(&s_misc[2], n_hot);
+    __threadfence();  // hot-hit stamps visible to rank 0 before barrier A
+    __syncthreads();
+    hs::cluster_arrive();  // barrier A
+
+    if (g == 0) {
+        hs::cluster_wait();
+        // ------------------------------------------------ rank 0: LRU update
+        int32_t *s_off = s_misc + 3;
+        if (tid == 0) {
+            int acc = 0, res = 0, hot = 0;
+            for (int q = 0; q < G; ++q) {
+                s_off[q] = acc;
+                acc += hs::dsmem_ld(hs::dsmem_map(&s_misc[0], q));
+                res += hs::dsmem_ld(hs::dsmem_map(&s_misc[1], q));
+                hot += hs::dsmem_ld(hs::dsmem_map(&s_misc[2], q));
+            }
+            s_off[G] = acc;
+            s_off[G + 1] = res;
+            s_off[G + 2] = hot;
+        }
+        __syncthreads();
+        const int n_miss = s_off[G], tot_res = s_off[G + 1], tot_hot = s_off[G + 2];
+        const bool leased = hblk[0] >= 0;
+        int served = 0;
+        if (n_miss > 0 || tot_hot > 0) {
+            // gather (position, list index) keys from every CTA's miss list
+            for (int q = 0; q < G; ++q) {
+                const int nq = s_off[q + 1] - s_off[q];
+                const uint32_t mj = hs::dsmem_map(s_mj, q), mp = hs::dsmem_map(s_mp, q);
+                for (int i = tid; i < nq; i += NT) {
+                    const int l = hs::dsmem_ld(mj + 4 * i);
+                    const int p = hs::dsmem_ld(mp + 4 * i);
+                    s_keys[s_off[q] + i] =
+                        ((unsigned long long)(uint32_t)p << 32) | (uint32_t)(q * chunk + l);
+                }
+            }
+            const int n2 = next_pow2(n_miss);
+            for (int i = n_miss + tid; i < n2; i += NT) s_keys[i] = ~0ull;
+            __syncthreads();
+            for (int k = 2; k <= n2; k <<= 1) {  // bitonic sort, ascending
+                for (int jj = k >> 1; jj > 0; jj >>= 1) {
+                    for (int i = tid; i < (n2 >> 1); i += NT) {
+                        const int lo = (i / jj) * 2 * jj + (i % jj), hi = lo + jj;
+                        const unsigned long long a = s_keys[lo], b = s_keys[hi];
+                        if ((a > b) == ((lo & k) == 0)) {
+                            s_keys[lo] = b;
+                            s_keys[hi] = a;
+                        }
+                    }
+                    __syncthreads();
+                }
+            }
+            // rank of each miss among distinct positions; repeats get -1
+            int m = 0;
+            for (int base = 0; base < n_miss; base += NT) {
+                const int i = base + tid;
+                int first = 0;
+                if (i < n_miss)
+                    first = (i == 0) || ((s_keys[i] >> 32) != (s_keys[i - 1] >> 32));
+                int tot;
+                const int pre = hs::block_scan_flag<NT>(first, s_warp, tot);
+                if (i < n_miss) s_rank[i] = first ? m + pre : -1;
+                m += tot;
+            }
+            // walk the LRU order: the first m unprotected slots are the victims,
+            // the remaining unprotected slots move to the front (in place)
+            int nu = 0;
+            const int mv = leased ? m : 0;
+            for (int base = 0; base < C; base += NT) {
+                const int i = base + tid;
+                int o = -1, u = 0;
+                if (i < C) {
+                    o = lru[i];
+                    u = stamp[o] < c;
+                }
+                int tot;
+                const int pre = hs::block_scan_flag<NT>(u, s_warp, tot);
+                if (u) {
+                    const int k = nu + pre;
+                    if (k < mv) s_victim[k] = o;
+                    else lru[k - mv] = o;
+                }
+                nu += tot;
+            }
+            const int mvict = min(mv, nu);
+            served = mvict;
+            __syncthreads();
+            // place the misses; tell each owner CTA its slot row (-1 = rejected)
+            for (int i = tid; i < n_miss; i += NT) {
+                const unsigned long long key = s_keys[i];
+                const int p = static_cast<int>(key >> 32), j = static_cast<int>(key & 0xffffffffu);
+                const int rk = s_rank[i];
+                int dst = -1;
+                if (rk < 0) {
+                    err |= HS_DEVERR_DUPLICATE;
+                } else if (rk >= mvict) {
+                    err |= HS_DEVERR_CAPACITY;
+                } else {
+                    const int v = s_victim[rk];
+                    const int old = tag[v];
+                    if (old >= 0) p2s[old] = -1;
+                    tag[v] = p;
+                    stamp[v] = c;
+                    p2s[p] = v;
+                    dst = hblk[v >> 6] * hs::kPage + (v & 63);
+                }
+                const int owner = j / chunk;
+                hs::dsmem_st(hs::dsmem_map(&s_src[j - owner * chunk], owner), dst);
+            }
+            __syncthreads();
+            // the slots stamped this step, in slot order, close the LRU order
+            int out = nu - mvict;
+            for (int base = 0; base < C; base += NT) {
+                const int s = base + tid;
+                const int f = (s < C) && stamp[s] == c;
+                int tot;
+                const int pre = hs::block_scan_flag<NT>(f, s_warp, tot);
+                if (f) lru[out + pre] = s;
+                out += tot;
+            }
+        }
+        if (tid == 0) {
+            P.clock[r] = c;
+            counts[bi * 3 + 0] = tot_res;
+            counts[bi * 3 + 1] = tot_hot;
+            counts[bi * 3 + 2] = served;
+        }
+        __threadfence();
+        __syncthreads();
+        hs::cluster_arrive();  // barrier B: miss slots published
+    }
+
+    // ---------------------------------------------- phase 2: resident and hot rows
+    {
+        const int nunits = nloc * V;
+        uint8_t *gdst = gathered + row0 * RB;
+        for (int base = tid; base < nunits; base += NT * UNROLL) {
+            uint4 v[UNROLL];
+            int act[UNROLL];
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                const int i = base + u * NT;
+                act[u] = 0;
+                if (i < nunits) {
+                    const int l = i / V, part = i - l * V;
+                    const int kd = s_kind[l];
+                    if (kd == KIND_RES || kd == KIND_HOT) {
+                        v[u] = hs::ld_stream_v4(P.rows + (size_t)s_src[l] * RB + part * 16);
+                        act[u] = 1;
+                    } else if (kd == KIND_NONE) {
+                        v[u] = make_uint4(0, 0, 0, 0);
+                        act[u] = 1;
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u)
+                if (act[u]) hs::st_v4(gdst + (size_t)(base + u * NT) * 16, v[u]);
+        }
+        for (int l = tid; l < nloc; l += NT) {
+            const int kd = s_kind[l];
+            if (kd == KIND_MISS) continue;
+            resolved[row0 + l] = kd == KIND_NONE ? -1 : s_src[l];
+            if (fp8) gscale[row0 + l] = kd == KIND_NONE ? 0.f : P.scales[s_src[l]];
+        }
+    }
+
+    if (g != 0) {
+        hs::cluster_wait();    // barrier A (long complete)
+        hs::cluster_arrive();  // barrier B
+    }
+    hs::cluster_wait();  // barrier B: rank 0 has placed every miss
+
+    // ---------------------------------------------- phase 3: miss rows from host
+    {
+        const int nm = s_misc[0];
+        uint8_t *gdst = gathered + row0 * RB;
+        const int nunits = nm * V;
+        for (int base = tid; base < nunits; base += NT * UNROLL) {
+            uint4 v[UNROLL];
+            int dst[UNROLL], l_[UNROLL], part_[UNROLL];
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                const int i = base + u * NT;
+                dst[u] = -2;
+                if (i < nunits) {
+                    const int mi = i / V, part = i - mi * V;
+                    const int l = s_mj[mi];
+                    l_[u] = l;
+                    part_[u] = part;
+                    dst[u] = s_src[l];
+                    if (dst[u] >= 0)
+                        v[u] = hs::ld_v4(P.host_rows + (size_t)s_hrow[l] * RB + part * 16);
+                    else
+                        v[u] = make_uint4(0, 0, 0, 0);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                if (dst[u] == -2) continue;
+                if (dst[u] >= 0) hs::st_v4(P.rows + (size_t)dst[u] * RB + part_[u] * 16, v[u]);
+                hs::st_v4(gdst + (size_t)l_[u] * RB + part_[u] * 16, v[u]);
+            }
+        }
+        for (int mi = tid; mi < nm; mi += NT) {
+            const int l = s_mj[mi];
+            const int d = s_src[l];
+            resolved[row0 + l] = d;
+            if (fp8) {
+                const float sc = d >= 0 ? P.host_scales[s_hrow[l]] : 0.f;
+                if (d >= 0) P.scales[d] = sc;
+                gscale[row0 + l] = sc;
+            }
+        }
+    }
+    if (err) atomicOr(P.err, err);
+}
+
+int pick_cluster(int K) {
+    // 8 CTAs per request (portable cluster size); fewer for short lists
+    int G = 8;
+    while (G > 1 && (K + G - 1) / G < 32) G >>= 1;
+    return G;
+}
+
+}  // namespace
+
+size_t hs_resolve_smem_bytes(int K, int G, int C) {
+    (void)C;
+    const int chunk = (K + G - 1) / G;
+    Smem L{chunk, next_pow2(K), K};
+    return L.total();
+}
+
+hs_status hs_resolve_prepare(hs_pool *pool) {
+    size_t mx = 0;
+    for (int K = 1; K <= pool->cfg.max_topk; ++K) {
+        const size_t b = hs_resolve_smem_bytes(K, pick_cluster(K), pool->cfg.hot_rows);
+        if (b > mx) mx = b;
+    }
+    if (mx > 200 * 1024) return HS_ERR_UNSUPPORTED;
+    HS_CUDA_TRY(cudaFuncSetAttribute(resolve_kernel<1152>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx));
+    HS_CUDA_TRY(cudaFuncSetAttribute(resolve_kernel<576>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx));
+    return HS_OK;
+}
+
+hs_status hs_launch_resolve(hs_pool *pool, int32_t B, const int32_t *req_ids, const int32_t *topk,
+                            int32_t K, int32_t *resolved, void *gathered, float *gscale,
+                            int32_t *counts, cudaStream_t stream) {
+    const int G = pick_cluster(K);
+    const int chunk = (K + G - 1) / G;
+    const size_t smem = hs_resolve_smem_bytes(K, G, pool->cfg.hot_rows);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(G, B, 1);
+    cfg.blockDim = dim3(NT, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = G;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const hs::DevPool P = pool->dev();
+    cudaError_t e;
+    if (pool->row_bytes == 1152)
+        e = cudaLaunchKernelEx(&cfg, resolve_kernel<1152>, P, req_ids, topk, (int)K, chunk, G,
+                               resolved, static_cast<uint8_t *>(gathered), gscale, counts);
+    else
+        e = cudaLaunchKernelEx(&cfg, resolve_kernel<576>, P, req_ids, topk, (int)K, chunk, G,
+                               resolved, static_cast<uint8_t *>(gathered), gscale, counts);
+    return e == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+}
+
+extern "C" hs_status hs_resolve_topk(hs_pool_t pool, int32_t B, const int32_t *d_req_ids,
+                                     const int32_t *d_topk_idx, int32_t K, int32_t *d_resolved,
+                                     void *d_gathered, float *d_gathered_scale, int32_t *d_counts,
+                                     void *stream) {
+    if (!pool || B < 0 || !d_req_ids || !d_topk_idx || !d_resolved || !d_gathered || !d_counts)
+        return HS_ERR_INVALID_ARG;
+    if (K < 1 || K > pool->cfg.max_topk || K > pool->cfg.hot_rows) return HS_ERR_CAPACITY;
+    if (B > 65535) return HS_ERR_INVALID_ARG;
+    const bool fp8 = pool->cfg.dtype == HS_FP8_E4M3_ROWSCALE;
+    if (fp8 != (d_gathered_scale != nullptr)) return HS_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(d_gathered) & 15u) != 0) return HS_ERR_INVALID_ARG;
+    if (B == 0) return HS_OK;
+    return hs_launch_resolve(pool, B, d_req_ids, d_topk_idx, K, d_resolved, d_gathered,
+                             d_gathered_scale, d_counts, static_cast<cudaStream_t>(stream));
+}

@@ -264,20 +264,22 @@ def topk_lists(w: Workload) -> Iterator[np.ndarray]:
 
 
 # ------------------------------------------------------------------ rows, q
-def fill_rows(dtype: str, rows, scales, seed: int, chunk_rows: int = 1 << 20):
+def fill_rows(dtype: str, rows, scales, seed: int, chunk_rows: int = 1 << 20, gen_device=None):
     """Fill `rows` (torch uint8 [n, row_bytes], any device) with N(0,1) latent rows.
 
     BF16: the float32 draws rounded to bfloat16. FP8: scale = amax/448 per row,
     codes = e4m3fn(x / scale) with round-to-nearest-even; the scale goes to
-    `scales` (torch float32 [n], same device) in a parallel array.
-    Deterministic for a given seed and device."""
+    `scales` (torch float32 [n]) in a parallel array. The draws are made on
+    `gen_device` (default: the device of `rows`) and copied; the values are
+    deterministic for a given seed and generating device."""
     import torch
     n = rows.shape[0]
-    g = torch.Generator(device=rows.device)
+    dev = torch.device(gen_device) if gen_device is not None else rows.device
+    g = torch.Generator(device=dev)
     g.manual_seed(seed)
     for a in range(0, n, chunk_rows):
         b = min(n, a + chunk_rows)
-        x = torch.randn((b - a, DIM), generator=g, device=rows.device, dtype=torch.float32)
+        x = torch.randn((b - a, DIM), generator=g, device=dev, dtype=torch.float32)
         if dtype == "bf16":
             rows[a:b].copy_(x.to(torch.bfloat16).view(torch.uint8))
         else:
