@@ -1,0 +1,433 @@
+"""Benchmark of the tiered sparse-MLA decode hot path on GB300.
+
+One step = one decode step of the whole path over one batch: hs_resolve_topk
+(fused resolve of 32 top-K lists against the tiered cache) followed by
+hs_sparse_mla_decode (attention over the 2048 selected latent rows per request).
+
+Workload: the fully resident configuration -- 32 requests x 131,072 tokens,
+64-token pages all GPU-resident, BF16 576-wide latent rows N(0,1), 128 heads,
+1 query token, top-K = 2048 (last 128 tokens + Zipf(1.0) over the rest),
+64 pregenerated decode steps cycled. L2 is flushed (a 256 MiB write) before
+every timed step; per-step CUDA events exclude the flush.
+
+Prints one JSON line. --impl reference times the CPU oracle instead (bounded
+sample of the same workload, on the host cores).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "resolved top-K rows/s & sparse-MLA decode steps/s; % of HBM/host-link roofline"
+WORKLOAD = "resident"
+WORKLOAD_DESC = ("fully resident: 32 requests x 131072-token context, 64-token pages all "
+                 "GPU-resident, BF16 576-wide latent rows, 128 heads, 1 query token, "
+                 "top-K 2048 (last 128 + Zipf(1.0)), hot buffer 4096 rows/request")
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("hbm_gbs"), d.get("bf16_tflops"), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def _traffic(kernel: str, src: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's
+    source is unchanged since the capture (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel)
+    if not d:
+        return None
+    sha = hashlib.sha256(open(os.path.join(ROOT, src), "rb").read()).hexdigest()[:16]
+    return d["dram_bytes_per_launch"] if d.get("source_sha") == sha else None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                self.out, _ = self.p.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+                self.out, _ = self.p.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (getattr(self, "out", "") or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def algorithmic(w, counts_sum):
+    """Algorithmic bytes / flops of one step (per-unit figures x units)."""
+    B, K, rb = w.B, w.K, w.row_bytes
+    rows = B * K
+    res, hot, miss = counts_sum
+    resolve_hbm = (res + hot) * rb + rows * rb + miss * rb + rows * 12
+    resolve_link = miss * rb
+    q = B * w.T * w.H * 576 * 2
+    out = B * w.T * w.H * 512 * 2 + B * w.T * w.H * 4
+    decode_bytes = rows * rb + q + out + rows * 8
+    flops = 2.0 * B * w.T * w.H * K * (576 + 512)
+    return resolve_hbm, resolve_link, decode_bytes, flops
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    import __graft_entry__ as g
+    g.build()
+    import tiered_sparse_mla_gb300 as hs
+    import workloads as W
+    from harness import GpuWorkload
+
+    w = W.WORKLOADS[WORKLOAD]
+    if args.batch != w.B:
+        w = w.scaled(B=args.batch)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        gw = GpuWorkload(w, stream=stream)
+        qs = [W.make_q(w, s, device="cuda") for s in range(w.steps)]
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+
+    def step(s, ev=None):
+        t = gw.topk[s % w.steps]
+        if ev is not None:
+            ev[0].record(stream)
+        gw.pool.resolve_topk(gw.req_ids, t, gw.resolved, gw.gathered, gw.gscale, gw.counts, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        gw.pool.sparse_mla_decode(qs[s % w.steps], gw.gathered, gw.gscale, gw.resolved, t,
+                                  gw.req_ids, w.sm_scale, gw.out, gw.lse, gw.workspace, stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    with torch.cuda.stream(stream):
+        for s in range(args.warmup):
+            flush.zero_()
+            step(s)
+    torch.cuda.synchronize()
+    assert gw.pool.get_error() == 0
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    cnt_sum = np.zeros(3, np.int64)
+    counts_acc = torch.zeros(3, dtype=torch.int64, device="cuda")
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with ClockSampler(local) as clk, torch.cuda.stream(stream):
+        torch.cuda.nvtx.range_push("timed_region")
+        for s in range(args.steps):
+            flush.zero_()
+            step(args.warmup + s, evs[s])
+            counts_acc += gw.counts.sum(0)
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if ws > 1:
+        dist.barrier()
+    assert gw.pool.get_error() == 0
+    cnt_sum = counts_acc.cpu().numpy()
+    t_res = [evs[s][0].elapsed_time(evs[s][1]) for s in range(args.steps)]
+    t_dec = [evs[s][1].elapsed_time(evs[s][2]) for s in range(args.steps)]
+    ms_step = (sum(t_res) + sum(t_dec)) / args.steps
+    if ws > 1:
+        tt = torch.tensor([ms_step], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step = float(tt.item())
+    steps_per_s = ws / (ms_step * 1e-3)
+    res_ms = sum(t_res) / args.steps
+    dec_ms = sum(t_dec) / args.steps
+    rows_per_s = ws * w.B * w.K / (res_ms * 1e-3)
+
+    per_step_counts = cnt_sum / args.steps
+    r_hbm, r_link, d_bytes, flops = algorithmic(w, per_step_counts)
+    hbm_peak, tf_peak, peak_kind = _peaks()
+    kernels = {
+        "resolve": {"ms": res_ms, "achieved": r_hbm / (res_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "peak": hbm_peak, "bound": "hbm", "bytes_per_launch": r_hbm,
+                    "traffic": _traffic("resolve", "tiered_sparse_mla_gb300/csrc/hs_resolve.cu")},
+        "decode": {"ms": dec_ms, "achieved": d_bytes / (dec_ms * 1e-3) / 1e9, "unit": "GB/s",
+                   "peak": hbm_peak, "bound": "hbm", "bytes_per_launch": d_bytes,
+                   "tflops": flops / (dec_ms * 1e-3) / 1e12,
+                   "traffic": _traffic("decode", "tiered_sparse_mla_gb300/csrc/hs_decode.cu")},
+    }
+    # the decode's roofline time is max(bytes / BW, flops / tensor peak)
+    t_bytes = d_bytes / (hbm_peak * 1e9)
+    t_flops = flops / (tf_peak * 1e12)
+    if t_flops > t_bytes:
+        kernels["decode"].update(bound="tensor", achieved=flops / (dec_ms * 1e-3) / 1e12,
+                                 unit="TFLOP/s", peak=tf_peak)
+    top = max(kernels, key=lambda k: kernels[k]["ms"])
+    kt = kernels[top]
+    roofline = {"kernel": top, "bound": kt["bound"], "achieved": round(kt["achieved"], 1),
+                "peak": kt["peak"], "unit": kt["unit"],
+                "frac": round(kt["achieved"] / kt["peak"], 4), "traffic": kt["traffic"],
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"}
+
+    # ---- end to end through the C ABI with host buffers (pinned), per step
+    e2e = run_e2e(args, gw, qs, stream, w)
+    launches = 2 + (1 if hs.hs_decode_workspace_bytes(w.B, w.T, w.H, w.K) > 0 else 0)
+    line = {
+        "metric": METRIC, "value": round(steps_per_s, 2), "unit": "decode steps/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC if w.B == 32 else f"{WORKLOAD_DESC} [batch {w.B}]",
+                   "global_batch": w.B * ws, "top_k": w.K,
+                   "heads": w.H, "query_tokens": w.T, "ctx": w.ctx,
+                   "parallelism": f"replicas x{ws} (requests sharded by rank, no collective)",
+                   "l2": "flushed (256 MiB write) before every timed step"},
+        "resolved_rows_per_s": round(rows_per_s, 1),
+        "resolve_ms": round(res_ms, 5), "decode_ms": round(dec_ms, 5),
+        "counts_per_step": {"resident": float(per_step_counts[0]), "hot": float(per_step_counts[1]),
+                            "miss": float(per_step_counts[2])},
+        "roofline": roofline,
+        "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
+                    for k, v in kernels.items()},
+        "e2e": e2e, "gpu_launches": launches * args.steps,
+        "clocks": clk.summary(), "wall_s": round(wall, 3),
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    gw.pool.close()
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, gw, qs, stream, w):
+    """Same step through the C ABI, inputs copied from pinned host memory and the
+    result (out, lse) read back to host memory inside the timed region."""
+    import torch
+    n = min(args.steps, 200)
+    topk_h = [gw.topk[s % w.steps].cpu().pin_memory() for s in range(w.steps)]
+    q_h = [qs[s % w.steps].cpu().pin_memory() for s in range(w.steps)]
+    out_h = torch.empty(gw.out.shape, dtype=gw.out.dtype).pin_memory()
+    lse_h = torch.empty(gw.lse.shape, dtype=gw.lse.dtype).pin_memory()
+    t_d = torch.empty_like(gw.topk[0])
+    q_d = torch.empty_like(qs[0])
+    h2d = topk_h[0].numel() * 4 + q_h[0].numel() * 2
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    with torch.cuda.stream(stream):
+        for s in range(3):
+            t_d.copy_(topk_h[s], non_blocking=True)
+            q_d.copy_(q_h[s], non_blocking=True)
+            gw.pool.resolve_topk(gw.req_ids, t_d, gw.resolved, gw.gathered, gw.gscale, gw.counts, stream)
+            gw.pool.sparse_mla_decode(q_d, gw.gathered, gw.gscale, gw.resolved, t_d, gw.req_ids,
+                                      w.sm_scale, gw.out, gw.lse, gw.workspace, stream)
+            out_h.copy_(gw.out, non_blocking=True)
+            lse_h.copy_(gw.lse, non_blocking=True)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for s in range(n):
+            t_d.copy_(topk_h[s % w.steps], non_blocking=True)
+            q_d.copy_(q_h[s % w.steps], non_blocking=True)
+            gw.pool.resolve_topk(gw.req_ids, t_d, gw.resolved, gw.gathered, gw.gscale, gw.counts, stream)
+            gw.pool.sparse_mla_decode(q_d, gw.gathered, gw.gscale, gw.resolved, t_d, gw.req_ids,
+                                      w.sm_scale, gw.out, gw.lse, gw.workspace, stream)
+            out_h.copy_(gw.out, non_blocking=True)
+            lse_h.copy_(gw.lse, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    ws, _, _ = _dist()
+    return {"value": round(ws / (ms * 1e-3), 2), "unit": "decode steps/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "note": "pinned host inputs (top-K lists, q) and outputs (out, lse); L2 not flushed"}
+
+
+# ------------------------------------------------------------------ CPU oracle
+class OracleSampler:
+    """The oracle, as it stands, on a bounded sample of the workload: a
+    sub-batch of `n_req` requests of the same shape (same context, top-K,
+    heads, own seeded lists and rows, generated on the host). Each step
+    resolves the whole sub-batch and attends `n_rows` query rows; the time is
+    extrapolated to the full batch (requests are independent and identical
+    in shape)."""
+
+    def __init__(self, w_full, n_req, threads):
+        import numpy as np
+        import torch
+        import oracle
+        import workloads as W
+        oracle.build()
+        self.np, self.torch, self.oracle, self.W = np, torch, oracle, W
+        self.full = w_full
+        self.w = w = w_full.scaled(B=n_req)
+        self.threads = threads
+        lay = W.layout(w)
+        pool = torch.empty((lay.n_gpu_blocks * 64, w.row_bytes), dtype=torch.uint8)
+        W.fill_rows(w.dtype, pool, None, W.row_seed(w, "gpu"))
+        self.ot = oracle.OracleTiers(
+            page_gpu=lay.page_gpu, page_host=lay.page_host, hot_blocks=lay.hot_blocks,
+            ctx_len=np.full(w.B, w.ctx, np.int32), pool_rows=pool.numpy(), pool_scales=None,
+            host_rows=np.zeros((64, w.row_bytes), np.uint8), host_scales=None,
+            hot_rows=w.hot_rows, max_ctx=w.ctx)
+        self.lists = list(W.topk_lists(w))
+
+    def step(self, s, n_rows):
+        np, torch, w = self.np, self.torch, self.w
+        topk = self.lists[s % len(self.lists)]
+        q_bits = self.W.make_q(w, s).view(torch.int16).numpy().view(np.uint16)
+        t0 = time.perf_counter()
+        res, gat, _, _, err = self.ot.resolve(np.arange(w.B), topk, nthreads=self.threads)
+        t1 = time.perf_counter()
+        n = w.B * w.T * w.H
+        idx = np.arange(min(n_rows, n))
+        sel = np.stack([idx // (w.T * w.H), (idx // w.H) % w.T, idx % w.H], 1).astype(np.int32)
+        self.oracle.sparse_mla_decode(q_bits, gat, None, res, topk, np.full(w.B, w.ctx, np.int32),
+                                      w.sm_scale, sel=sel, nthreads=self.threads)
+        t2 = time.perf_counter()
+        full = self.full
+        extrap = (t1 - t0) * full.B / w.B + (t2 - t1) * (full.B * full.T * full.H) / len(idx)
+        return extrap, t2 - t0, t1 - t0, (t2 - t1) / len(idx)
+
+
+def cpu_baseline(w, args):
+    import oracle
+    oracle.build()
+    threads = oracle.max_threads()
+    n_req = 4
+    smp = OracleSampler(w, n_req, threads)
+    per, spent, s = [], 0.0, 0
+    while s < len(smp.lists) and (spent < args.cpu_seconds or s < 1):
+        e, m, _, _ = smp.step(s, n_req * w.T * w.H)
+        per.append(e)
+        spent += m
+        s += 1
+    v = len(per) / sum(per)
+    return {"value": round(v, 5), "unit": "decode steps/s", "cores": threads, "kind": "oracle",
+            "sample": (f"{s} decode steps of a {n_req}-request sub-batch of the same workload "
+                       f"(resolve and attention of all {n_req * w.T * w.H} query rows), "
+                       f"extrapolated to {w.B} requests; {spent:.1f} s of CPU work")}
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle as it stands, same workload and metric;
+    each step a bounded sample (one request resolved, some query rows attended)
+    sized so that the whole run ends within a few minutes."""
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    import oracle
+    import workloads as W
+    oracle.build()
+    w = W.WORKLOADS[WORKLOAD]
+    threads = oracle.max_threads()
+    smp = OracleSampler(w, 1, threads)
+    budget = 150.0 / (args.steps + args.warmup)
+    _, _, t_res, t_row = smp.step(0, 8)
+    n_rows = int(max(1, min(w.T * w.H, (budget - t_res) / max(t_row, 1e-9))))
+    times = []
+    for s in range(args.warmup + args.steps):
+        e, _, _, _ = smp.step(s, n_rows)
+        if s >= args.warmup:
+            times.append(e)
+    ms = 1e3 * sum(times) / len(times)
+    v = 1e3 / ms
+    sample = (f"each step: resolve of 1 of {w.B} requests and attention of {n_rows} of its "
+              f"{w.T * w.H} query rows, extrapolated to the full {w.B}-request step")
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 5), "unit": "decode steps/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC, "global_batch": w.B, "top_k": w.K},
+            "cpu_baseline": {"value": round(v, 5), "unit": "decode steps/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(v, 5), "unit": "decode steps/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU work spent on the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=32,
+                    help="requests per step (32 = the workload; smaller only for profiling)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

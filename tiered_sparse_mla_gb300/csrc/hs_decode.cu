@@ -1,91 +1,660 @@
-// hs_decode.cu -- sparse MLA decode over the gathered top-K latent rows.
+// hs_decode.cu -- sparse MLA decode over the gathered top-K latent rows, on
+// tcgen05 tensor cores (sm_103a).
 //
 // Attention restricted to the K rows the indexer selected ("vLLM GLM 5.3 优化：
 // 混合 HiSparse 卸载", section 解决 KV 缓存内存压力; "vLLM Hybrid HiSparse：稀疏MLA
 // 破解长上下文显存瓶颈", section 稀疏MLA的核心思想). MLA keeps one 576-wide latent
-// row per token; the key is the whole row and the value its first 512 elements.
+// row per token: the key is the whole row, the value its first 512 elements.
 // Query token t of a request sits at position L - T + t and sees entries whose
-// position is <= that (MTP draft tokens share one top-K list).
+// position is <= that (MTP draft tokens share one top-K list, 与 vLLM 栈的集成).
+//
+// All H*T query rows of a request share the same K rows, so QK^T and PV are
+// dense contractions: S[128 x 64] = Q[128 x 576] K^T, O[128 x 256] += P V.
+//
+// CTA = (request, 128-row M tile, 256-column half of the output, KV split).
+//   warp 0   TMA producer: Q once (9 boxes of 64 columns, 128B swizzle), then
+//            64-key x 64-column chunks of the gathered rows through a ring
+//            (BF16: straight into the ring; FP8: into a staging ring);
+//   warps 2-3 (FP8 only) convert e4m3 chunks to f16 with the row scale
+//            folded in, and Q from bf16 to f16 once;
+//   warp 1   MMA issuer (one thread): S_i = Q K_i^T into one of two TMEM S
+//            buffers, then O += P_i V_i. V is the same smem chunk as K, read
+//            through an MN-major descriptor, so no transpose is stored;
+//   warps 4-7 softmax, one thread per query row (TMEM lane): masking, online
+//            softmax with a conditional rescale (the running max only moves
+//            when a tile's max exceeds it by 2^8, so O in TMEM is rarely
+//            touched), P to smem, epilogue.
+// TMEM: O half 256 columns + 2 x 64 S columns (512 allocated). A full 512-wide
+// O would leave no TMEM for S, so the two output halves run in two CTAs that
+// both compute S (576-deep); the gathered rows are read from L2 twice.
+// Every mbarrier wait is bounded in time; on expiry the kernel sets
+// HS_DEVERR_TIMEOUT, drains its own copies and MMAs and returns.
+#include <cuda.h>
 #include <cuda_bf16.h>
-#include <cuda_fp8.h>
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
 
+#include <climits>
 #include <cstdint>
 
 #include "hs_internal.cuh"
+#include "hs_tc.cuh"
 
 namespace {
 
-constexpr int SIMPLE_WARPS = 8;
+using namespace hs::tc;
 
-// One warp per query row (b, t, h); lanes own latent elements d = 32*i + lane.
+constexpr int NTHR = 256;
+constexpr int BM = 128, BN = 64, NCH = 9, NVC = 4;
+constexpr int QCH_BYTES = BM * 128;  // 128 rows x 64 columns x 2 B
+constexpr int KCH_BYTES = BN * 128;  // 64 keys x 64 columns x 2 B
+constexpr int FCH_BYTES = BN * 64;   // 64 keys x 64 e4m3 codes
+constexpr int P_BYTES = BM * 128;    // 128 rows x 64 keys x 2 B
+constexpr float TAU2 = 8.f;          // rescale threshold, log2 units
+constexpr uint32_t TMEM_COLS = 512, TM_O = 0, TM_S = 256;
+
 template <bool FP8>
-__global__ void __launch_bounds__(SIMPLE_WARPS * 32)
-decode_rowwise_kernel(const __nv_bfloat16 *__restrict__ q, const uint8_t *__restrict__ gathered,
-                      const float *__restrict__ gscale, const int32_t *__restrict__ resolved,
-                      const int32_t *__restrict__ topk, const int32_t *__restrict__ req_ids,
-                      const int32_t *__restrict__ ctx, int max_req, int T, int H, int K,
-                      float sm_scale, __nv_bfloat16 *__restrict__ out, float *__restrict__ lse) {
-    constexpr int NI = hs::kDim / 32;   // 18 elements per lane
-    constexpr int NV = hs::kNope / 32;  // 16 value elements per lane
-    const int lane = threadIdx.x & 31;
-    const int h = blockIdx.x * SIMPLE_WARPS + (threadIdx.x >> 5);
-    const int t = blockIdx.y, b = blockIdx.z;
-    if (h >= H) return;
-    const int r = req_ids[b];
-    const int Lr = (r >= 0 && r < max_req) ? ctx[r] : 0;
-    const int pos = Lr - T + t;
-    const size_t qrow = ((size_t)b * T + t) * H + h;
-    float qv[NI], acc[NV];
-#pragma unroll
-    for (int i = 0; i < NI; ++i) qv[i] = __bfloat162float(q[qrow * hs::kDim + 32 * i + lane]);
-#pragma unroll
-    for (int i = 0; i < NV; ++i) acc[i] = 0.f;
-    float m = -INFINITY, l = 0.f;
-    for (int j = 0; j < K; ++j) {
-        const size_t bj = (size_t)b * K + j;
-        if (resolved[bj] < 0 || topk[bj] > pos) continue;
-        float kv[NI];
-        if (FP8) {
-            const uint8_t *row = gathered + bj * hs::kDim;
-            const float sc = gscale[bj];
-#pragma unroll
-            for (int i = 0; i < NI; ++i) {
-                __nv_fp8_e4m3 x;
-                x.__x = row[32 * i + lane];
-                kv[i] = static_cast<float>(x) * sc;
-            }
-        } else {
-            const __nv_bfloat16 *row = reinterpret_cast<const __nv_bfloat16 *>(gathered) + bj * hs::kDim;
-#pragma unroll
-            for (int i = 0; i < NI; ++i) kv[i] = __bfloat162float(row[32 * i + lane]);
-        }
-        float s = 0.f;
-#pragma unroll
-        for (int i = 0; i < NI; ++i) s = fmaf(qv[i], kv[i], s);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        s *= sm_scale;
-        const float mn = fmaxf(m, s);
-        const float alpha = expf(m - mn), p = expf(s - mn);
-        l = l * alpha + p;
-#pragma unroll
-        for (int i = 0; i < NV; ++i) acc[i] = fmaf(acc[i], alpha, p * kv[i]);
-        m = mn;
+struct Cfg {
+    static constexpr int RING = FP8 ? 5 : 6;
+    static constexpr int FRING = FP8 ? 4 : 0;
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_RING = OFF_Q + NCH * QCH_BYTES;
+    static constexpr int OFF_P = OFF_RING + RING * KCH_BYTES;
+    static constexpr int OFF_F = OFF_P + P_BYTES;
+    static constexpr int OFF_BAR = OFF_F + FRING * FCH_BYTES;
+    static constexpr int B_QFULL = 0, B_QREADY = 1, B_DRAIN = 2, B_RFULL = 3;
+    static constexpr int B_REMPTY = B_RFULL + RING, B_SFULL = B_REMPTY + RING;
+    static constexpr int B_PFULL = B_SFULL + 2, B_PVDONE = B_PFULL + 1;
+    static constexpr int B_FFULL = B_PVDONE + 1, B_FEMPTY = B_FFULL + FRING;
+    static constexpr int NBAR = B_FEMPTY + FRING;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // [0] TMEM base, [1] abort flag
+    static constexpr int OFF_KPOS = OFF_MISC + 16;       // int32 [2][64]
+    static constexpr int SMEM = OFF_KPOS + 2 * BN * 4;
+    static constexpr int SMEM_ALLOC = SMEM + 1024;       // room to align the base to 1 KiB
+    static_assert(OFF_RING % 1024 == 0 && OFF_P % 1024 == 0 && OFF_F % 1024 == 0, "align");
+    static_assert(SMEM_ALLOC <= 232448, "shared memory");
+};
+
+struct DecParams {
+    const int32_t *resolved, *topk, *req_ids, *ctx;
+    const float *gscale;
+    __nv_bfloat16 *out;
+    float *lse, *ws_o, *ws_lse;
+    uint32_t *err;
+    int B, T, H, K, M, nsplit, kps, max_req;
+    float scale_log2;
+};
+
+__device__ __forceinline__ void st_shared_v4(uint32_t a, uint32_t x, uint32_t y, uint32_t z,
+                                             uint32_t w) {
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(a)
+                 : "memory");
+    return v;
+}
+
+// TMEM load of 32 columns whose registers only become valid after the wait;
+// the wait takes them as operands so no use can be scheduled before it.
+#define HS_TMEM_LD32(taddr, r)                                                                    \
+    asm volatile(                                                                                 \
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"  \
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"        \
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),    \
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),             \
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),          \
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),          \
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),          \
+          "=r"(r[31])                                                                             \
+        : "r"(taddr)                                                                              \
+        : "memory")
+#define HS_TMEM_WAIT_LD32(r)                                                                      \
+    asm volatile("tcgen05.wait::ld.sync.aligned;"                                                 \
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),        \
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),      \
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),  \
+                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),  \
+                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),  \
+                   "+r"(r[30]), "+r"(r[31])::"memory")
+
+template <bool FP8>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if (FP8) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
+    } else {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
     }
-    const float inv = l > 0.f ? 1.f / l : 0.f;
+}
+
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+    uint32_t r;
+    const uint16_t v = static_cast<uint16_t>(two_codes);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, __half2 s) {
+    __half2 h = *reinterpret_cast<__half2 *>(&a);
+    h = __hmul2(h, s);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+    const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// The chunk sequence shared by producer, converters and MMA issuer:
+// QK chunks of tile i (9), then the PV chunks of tile i-1 (the 4 V chunks of
+// this CTA's output half). `f(tile, chunk)` returns false to stop.
+template <typename F>
+__device__ __forceinline__ bool for_each_chunk(int ntiles, int half, F &&f) {
+    for (int i = 0; i <= ntiles; ++i) {
+        if (i < ntiles)
+            for (int c = 0; c < NCH; ++c)
+                if (!f(i, c)) return false;
+        if (i >= 1)
+            for (int c = half * NVC; c < half * NVC + NVC; ++c)
+                if (!f(i - 1, c)) return false;
+    }
+    return true;
+}
+
+template <bool FP8>
+__global__ void __launch_bounds__(NTHR, 1)
+decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const DecParams p) {
+    using C = Cfg<FP8>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = hs::smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int half = blockIdx.x & 1, split = blockIdx.x >> 1, mt = blockIdx.y, b = blockIdx.z;
+    const int k0 = split * p.kps, k1 = min(p.K, k0 + p.kps);
+    const int ntiles = (k1 - k0 + BN - 1) / BN;
+    volatile int32_t *misc = reinterpret_cast<volatile int32_t *>(smem + C::OFF_MISC);
+    int32_t *kpos = reinterpret_cast<int32_t *>(smem + C::OFF_KPOS);
+    const uint32_t sQ = base + C::OFF_Q, sR = base + C::OFF_RING, sP = base + C::OFF_P;
+    const uint32_t sF = base + C::OFF_F;
+    auto bar = [&](int i) { return base + C::OFF_BAR + 8u * (uint32_t)i; };
+    auto fail = [&]() {
+        misc[1] = 1;
+        atomicOr(p.err, HS_DEVERR_TIMEOUT);
+    };
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::B_QFULL), 1);
+        mbar_init(bar(C::B_QREADY), 64);
+        mbar_init(bar(C::B_DRAIN), 1);
+        for (int i = 0; i < C::RING; ++i) {
+            mbar_init(bar(C::B_RFULL + i), FP8 ? 64 : 1);
+            mbar_init(bar(C::B_REMPTY + i), 1);
+        }
+        mbar_init(bar(C::B_SFULL), 1);
+        mbar_init(bar(C::B_SFULL + 1), 1);
+        mbar_init(bar(C::B_PFULL), 128);
+        mbar_init(bar(C::B_PVDONE), 1);
+        for (int i = 0; i < C::FRING; ++i) {
+            mbar_init(bar(C::B_FFULL + i), 1);
+            mbar_init(bar(C::B_FEMPTY + i), 64);
+        }
+        misc[1] = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(base + C::OFF_MISC, TMEM_COLS);
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = static_cast<uint32_t>(misc[0]);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            mbar_expect_tx(bar(C::B_QFULL), NCH * QCH_BYTES);
+            for (int c = 0; c < NCH; ++c)
+                tma_load_3d(sQ + c * QCH_BYTES, &tm_q, 64 * c, mt * BM, b, bar(C::B_QFULL));
+            constexpr int NS = FP8 ? C::FRING : C::RING;
+            int slot = 0, issued = 0;
+            uint32_t ph = 0;
+            const bool ok = for_each_chunk(ntiles, half, [&](int tile, int c) {
+                const uint32_t empty = bar((FP8 ? C::B_FEMPTY : C::B_REMPTY) + slot);
+                const uint32_t full = bar((FP8 ? C::B_FFULL : C::B_RFULL) + slot);
+                if (!mbar_wait(empty, ph ^ 1) || misc[1]) return false;
+                if (FP8) {
+                    mbar_expect_tx(full, FCH_BYTES);
+                    tma_load_3d(sF + slot * FCH_BYTES, &tm_k, 64 * c, k0 + tile * BN, b, full);
+                } else {
+                    mbar_expect_tx(full, KCH_BYTES);
+                    tma_load_3d(sR + slot * KCH_BYTES, &tm_k, 64 * c, k0 + tile * BN, b, full);
+                }
+                ++issued;
+                if (++slot == NS) {
+                    slot = 0;
+                    ph ^= 1;
+                }
+                return true;
+            });
+            if (!ok) {
+                fail();
+                // let the copies this thread started land before the CTA exits
+                mbar_wait(bar(C::B_QFULL), 0);
+                for (int k = issued - 1; k >= 0 && k >= issued - NS; --k)
+                    mbar_wait(bar((FP8 ? C::B_FFULL : C::B_RFULL) + k % NS), (k / NS) & 1);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t AB = FP8 ? 0u : 1u;
+            constexpr uint32_t ID_QK = idesc_f16(AB, 0, BM, BN);
+            constexpr uint32_t ID_PV = idesc_f16(AB, 1, BM, BN);
+            bool ok = mbar_wait(bar(FP8 ? C::B_QREADY : C::B_QFULL), 0);
+            tc_fence_after();
+            int slot = 0;
+            uint32_t ph = 0;
+            for (int i = 0; i <= ntiles && ok; ++i) {
+                if (i < ntiles) {
+                    const uint32_t dS = tmem + TM_S + (uint32_t)(i & 1) * BN;
+                    for (int c = 0; c < NCH && ok; ++c) {
+                        if (!mbar_wait(bar(C::B_RFULL + slot), ph)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
 #pragma unroll
-    for (int i = 0; i < NV; ++i) out[qrow * hs::kNope + 32 * i + lane] = __float2bfloat16_rn(acc[i] * inv);
-    if (lane == 0) lse[qrow] = l > 0.f ? m + logf(l) : -INFINITY;
+                        for (int k = 0; k < 4; ++k) {
+                            const uint64_t a = desc_sw128(sQ + c * QCH_BYTES + k * 32, 16, 1024);
+                            const uint64_t bd = desc_sw128(sR + slot * KCH_BYTES + k * 32, 16, 1024);
+                            mma_f16(dS, a, bd, ID_QK, (c | k) != 0);
+                        }
+                        mma_commit(bar(C::B_REMPTY + slot));
+                        if (++slot == C::RING) {
+                            slot = 0;
+                            ph ^= 1;
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(bar(C::B_SFULL + (i & 1)));
+                }
+                if (i >= 1) {
+                    if (!mbar_wait(bar(C::B_PFULL), (i - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int c = 0; c < NVC && ok; ++c) {
+                        if (!mbar_wait(bar(C::B_RFULL + slot), ph)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t a = desc_sw128(sP + kk * 32, 16, 1024);
+                            const uint64_t bd =
+                                desc_sw128(sR + slot * KCH_BYTES + kk * 2048, KCH_BYTES, 1024);
+                            mma_f16(tmem + TM_O + 64 * c, a, bd, ID_PV, (i > 1) || (kk > 0));
+                        }
+                        mma_commit(bar(C::B_REMPTY + slot));
+                        if (++slot == C::RING) {
+                            slot = 0;
+                            ph ^= 1;
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(bar(C::B_PVDONE));
+                }
+                if (misc[1]) ok = false;
+            }
+            if (!ok) fail();
+            // every MMA issued above has finished before TMEM and smem are released
+            mma_commit(bar(C::B_DRAIN));
+            mbar_wait(bar(C::B_DRAIN), 0);
+        }
+    } else if (warp < 4) {
+        // ------------------------------------------------------------ FP8 converters
+        if (FP8) {
+            const int ct = threadIdx.x - 64;  // 0..63: one key row per chunk
+            bool ok = mbar_wait(bar(C::B_QFULL), 0);
+            if (ok) {
+                for (int q = ct; q < NCH * QCH_BYTES / 16; q += 64) {
+                    const uint4 v = ld_shared_v4(sQ + q * 16);
+                    st_shared_v4(sQ + q * 16, bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y),
+                                 bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+                }
+                fence_proxy_async();
+            } else {
+                fail();
+            }
+            mbar_arrive(bar(C::B_QREADY));
+            int fslot = 0, slot = 0, cur_tile = -1;
+            uint32_t fph = 0, ph = 0;
+            __half2 s2 = __float2half2_rn(0.f);
+            const float *gs = p.gscale + (size_t)b * p.K;
+            ok = ok && for_each_chunk(ntiles, half, [&](int tile, int c) {
+                if (tile != cur_tile) {
+                    cur_tile = tile;
+                    const int j = k0 + tile * BN + ct;
+                    s2 = __float2half2_rn(j < p.K ? gs[j] : 0.f);
+                }
+                if (!mbar_wait(bar(C::B_FFULL + fslot), fph) || misc[1]) return false;
+                const uint32_t src = sF + fslot * FCH_BYTES + ct * 64;
+                uint4 raw4[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) raw4[q] = ld_shared_v4(src + 16 * q);
+                mbar_arrive(bar(C::B_FEMPTY + fslot));
+                if (++fslot == C::FRING) {
+                    fslot = 0;
+                    fph ^= 1;
+                }
+                if (!mbar_wait(bar(C::B_REMPTY + slot), ph ^ 1)) return false;
+                const uint32_t dst = sR + slot * KCH_BYTES + ct * 128;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {  // 16 codes -> 16 f16 = two 16-byte chunks
+                    const uint32_t w[4] = {raw4[q].x, raw4[q].y, raw4[q].z, raw4[q].w};
+                    uint32_t h[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        h[2 * e] = hmul2_u32(e4m3x2_to_f16x2(w[e] & 0xffffu), s2);
+                        h[2 * e + 1] = hmul2_u32(e4m3x2_to_f16x2(w[e] >> 16), s2);
+                    }
+                    const int c0 = 2 * q, c1 = 2 * q + 1;
+                    st_shared_v4(dst + ((c0 ^ (ct & 7)) << 4), h[0], h[1], h[2], h[3]);
+                    st_shared_v4(dst + ((c1 ^ (ct & 7)) << 4), h[4], h[5], h[6], h[7]);
+                }
+                fence_proxy_async();
+                mbar_arrive(bar(C::B_RFULL + slot));
+                if (++slot == C::RING) {
+                    slot = 0;
+                    ph ^= 1;
+                }
+                return true;
+            });
+            if (!ok) fail();
+        }
+    } else {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int wq = warp - 4;
+        const int row = wq * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const int mg = mt * BM + row;
+        const bool vrow = mg < p.M;
+        const int r = p.req_ids[b];
+        const int L = (r >= 0 && r < p.max_req) ? p.ctx[r] : 0;
+        const int t = vrow ? mg / p.H : 0;
+        const int pos = L - p.T + t;
+        const int32_t *res_b = p.resolved + (size_t)b * p.K;
+        const int32_t *top_b = p.topk + (size_t)b * p.K;
+        float m2 = -INFINITY, l = 0.f;
+        bool ok = true;
+        // every softmax thread runs all ntiles iterations (the named barrier is
+        // not bounded in time); after a failed wait the work is skipped
+        for (int i = 0; i < ntiles; ++i) {
+            if (row < BN) {
+                const int j = k0 + i * BN + row;
+                int kp = INT_MAX;
+                if (j < k1 && res_b[j] >= 0) kp = top_b[j];
+                kpos[(i & 1) * BN + row] = kp;
+            }
+            named_bar_sync(1, 128);
+            if (!ok) continue;
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SFULL + (i & 1)), (i >> 1) & 1));
+            if (!ok) continue;
+            tc_fence_after();
+            uint32_t ra[32], rb[32];
+            const uint32_t tS = tmem + lane_off + TM_S + (uint32_t)(i & 1) * BN;
+            HS_TMEM_LD32(tS, ra);
+            HS_TMEM_LD32(tS + 32, rb);
+            HS_TMEM_WAIT_LD32(ra);
+            HS_TMEM_WAIT_LD32(rb);
+            float s[64];
+            float tmax = -INFINITY;
+            const int32_t *kp = kpos + (i & 1) * BN;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                const float raw_s = __uint_as_float(j < 32 ? ra[j] : rb[j - 32]);
+                const float v = kp[j] <= pos ? raw_s * p.scale_log2 : -INFINITY;
+                s[j] = v;
+                tmax = fmaxf(tmax, v);
+            }
+            if (i > 0) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_PVDONE), (i - 1) & 1));
+                if (!ok) continue;
+                tc_fence_after();
+            }
+            if (i == 0) {
+                m2 = tmax;
+            } else {
+                const bool need = tmax > m2 + TAU2;
+                if (__any_sync(0xffffffffu, need)) {
+                    const float alpha = need ? exp2f(m2 - tmax) : 1.f;
+                    if (need) {
+                        l *= alpha;
+                        m2 = tmax;
+                    }
+#pragma unroll 1
+                    for (int cc = 0; cc < 8; ++cc) {
+                        uint32_t o[32];
+                        const uint32_t tO = tmem + lane_off + TM_O + 32 * cc;
+                        HS_TMEM_LD32(tO, o);
+                        HS_TMEM_WAIT_LD32(o);
+                        float f[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(o[e]) * alpha;
+                        tmem_st32(tO, f);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            const float mref = (m2 == -INFINITY) ? 0.f : m2;
+            float lsum = 0.f;
+            uint32_t pk[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const float a = exp2f(s[2 * e] - mref), c = exp2f(s[2 * e + 1] - mref);
+                lsum += a + c;
+                pk[e] = pack2<FP8>(a, c);
+            }
+            l += lsum;
+            const uint32_t prow = sP + row * 128;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                st_shared_v4(prow + ((q ^ (row & 7)) << 4), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
+                             pk[4 * q + 3]);
+            fence_proxy_async();
+            tc_fence_before();
+            mbar_arrive(bar(C::B_PFULL));
+        }
+        if (ok && ntiles > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_PVDONE), (ntiles - 1) & 1));
+            tc_fence_after();
+        }
+        if (!ok) fail();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const size_t orow = (size_t)b * p.M + mg;
+        if (ok) {
+#pragma unroll 1
+            for (int cc = 0; cc < 8; ++cc) {
+                uint32_t o[32];
+                HS_TMEM_LD32(tmem + lane_off + TM_O + 32 * cc, o);
+                HS_TMEM_WAIT_LD32(o);
+                if (!vrow) continue;
+                const int col = half * 256 + 32 * cc;
+                if (p.nsplit == 1) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * 512 + col);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            w[e] = pack2<false>(__uint_as_float(o[8 * q + 2 * e]) * inv,
+                                                __uint_as_float(o[8 * q + 2 * e + 1]) * inv);
+                        dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                } else {
+                    float4 *dst = reinterpret_cast<float4 *>(
+                        p.ws_o + (((size_t)split * p.B + b) * p.M + mg) * 512 + col);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        dst[q] = make_float4(__uint_as_float(o[4 * q]) * inv,
+                                             __uint_as_float(o[4 * q + 1]) * inv,
+                                             __uint_as_float(o[4 * q + 2]) * inv,
+                                             __uint_as_float(o[4 * q + 3]) * inv);
+                }
+            }
+        }
+        if (vrow && half == 0) {
+            const float lse = (ok && l > 0.f) ? (m2 + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+            if (p.nsplit == 1)
+                p.lse[orow] = lse;
+            else
+                p.ws_lse[((size_t)split * p.B + b) * p.M + mg] = lse;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// Merges the KV-split partials: out = sum_s w_s O_s / sum_s w_s, w_s = exp(lse_s - max).
+__global__ void __launch_bounds__(256)
+combine_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_lse, int nsplit,
+               int rows, __nv_bfloat16 *__restrict__ out, float *__restrict__ lse) {
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    float mx = -INFINITY;
+    for (int s = 0; s < nsplit; ++s) mx = fmaxf(mx, ws_lse[(size_t)s * rows + row]);
+    float acc[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+    float wsum = 0.f;
+    if (mx != -INFINITY) {
+        for (int s = 0; s < nsplit; ++s) {
+            const float ls = ws_lse[(size_t)s * rows + row];
+            if (ls == -INFINITY) continue;
+            const float w = __expf(ls - mx);
+            wsum += w;
+            const float4 *src = reinterpret_cast<const float4 *>(ws_o + ((size_t)s * rows + row) * 512);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 v = src[lane + 32 * q];
+                acc[4 * q] += w * v.x;
+                acc[4 * q + 1] += w * v.y;
+                acc[4 * q + 2] += w * v.z;
+                acc[4 * q + 3] += w * v.w;
+            }
+        }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    uint2 *dst = reinterpret_cast<uint2 *>(out + (size_t)row * 512);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        dst[lane + 32 * q] = make_uint2(pack2<false>(acc[4 * q] * inv, acc[4 * q + 1] * inv),
+                                        pack2<false>(acc[4 * q + 2] * inv, acc[4 * q + 3] * inv));
+    if (lane == 0) lse[row] = wsum > 0.f ? mx + __logf(wsum) : -INFINITY;
+}
+
+// ---------------------------------------------------------------- host side
+struct Plan {
+    int M, mtiles, nsplit, kps;
+    size_t ws_o_bytes, ws_bytes;
+};
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!cached[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+Plan make_plan(int B, int T, int H, int K) {
+    Plan pl{};
+    pl.M = T * H;
+    pl.mtiles = (pl.M + BM - 1) / BM;
+    const int tiles = (K + BN - 1) / BN;
+    const int base = B * pl.mtiles * 2;
+    int ns = base > 0 ? sm_count() / base : 1;
+    if (ns < 1) ns = 1;
+    const int max_ns = tiles / 2 > 1 ? tiles / 2 : 1;  // at least two key tiles per split
+    if (ns > max_ns) ns = max_ns;
+    const int per = (tiles + ns - 1) / ns;
+    pl.kps = per * BN;
+    pl.nsplit = (K + pl.kps - 1) / pl.kps;
+    if (pl.nsplit > 1) {
+        const size_t rows = (size_t)pl.nsplit * B * pl.M;
+        pl.ws_o_bytes = (rows * 512 * sizeof(float) + 255) & ~size_t(255);
+        pl.ws_bytes = pl.ws_o_bytes + ((rows * sizeof(float) + 255) & ~size_t(255));
+    }
+    return pl;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+// 3-D map [batch][rows][inner] with a (box_inner x box_rows x 1) box.
+bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, uint64_t inner,
+              uint64_t rows, uint64_t batch, uint64_t row_bytes, uint32_t box_inner,
+              uint32_t box_rows, CUtensorMapSwizzle sw) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {inner, rows, batch};
+    cuuint64_t strides[2] = {row_bytes, row_bytes * rows};
+    cuuint32_t box[3] = {box_inner, box_rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, dt, 3, const_cast<void *>(ptr), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool FP8>
+hs_status prepare_kernel() {
+    static bool done = false;
+    if (!done) {
+        HS_CUDA_TRY(cudaFuncSetAttribute(decode_tc_kernel<FP8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg<FP8>::SMEM_ALLOC));
+        done = true;
+    }
+    return HS_OK;
 }
 
 }  // namespace
 
 extern "C" size_t hs_decode_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t K) {
-    (void)B;
-    (void)T;
-    (void)H;
-    (void)K;
-    return 0;
+    if (B < 1 || T < 1 || H < 1 || K < 1) return 0;
+    return make_plan(B, T, H, K).ws_bytes;
 }
 
 extern "C" hs_status hs_sparse_mla_decode(hs_pool_t pool, int32_t B, int32_t T, int32_t H, int32_t K,
@@ -94,27 +663,67 @@ extern "C" hs_status hs_sparse_mla_decode(hs_pool_t pool, int32_t B, int32_t T, 
                                           const int32_t *d_topk_idx, const int32_t *d_req_ids,
                                           float sm_scale, void *d_out, float *d_lse,
                                           void *d_workspace, size_t ws_bytes, void *stream) {
-    (void)d_workspace;
-    (void)ws_bytes;
     if (!pool || !d_q || !d_gathered || !d_resolved || !d_topk_idx || !d_req_ids || !d_out || !d_lse)
         return HS_ERR_INVALID_ARG;
-    if (B < 0 || T < 1 || H < 1 || K < 1 || B > 65535 || T > 65535 || H * T > 128 * 64)
+    if (B < 0 || T < 1 || H < 1 || K < 1 || B > 65535 || (int64_t)T * H > (int64_t)BM * 65535)
         return HS_ERR_INVALID_ARG;
     const bool fp8 = pool->cfg.dtype == HS_FP8_E4M3_ROWSCALE;
     if (fp8 != (d_gathered_scale != nullptr)) return HS_ERR_INVALID_ARG;
+    if (((uintptr_t)d_q | (uintptr_t)d_gathered | (uintptr_t)d_out) & 15u) return HS_ERR_INVALID_ARG;
     if (B == 0) return HS_OK;
-    const dim3 grid((H + SIMPLE_WARPS - 1) / SIMPLE_WARPS, T, B);
+    const Plan pl = make_plan(B, T, H, K);
+    if (pl.nsplit > 1 && (!d_workspace || ws_bytes < pl.ws_bytes || ((uintptr_t)d_workspace & 255u)))
+        return HS_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const auto *q = static_cast<const __nv_bfloat16 *>(d_q);
-    const auto *g = static_cast<const uint8_t *>(d_gathered);
-    auto *o = static_cast<__nv_bfloat16 *>(d_out);
-    if (fp8)
-        decode_rowwise_kernel<true><<<grid, SIMPLE_WARPS * 32, 0, s>>>(
-            q, g, d_gathered_scale, d_resolved, d_topk_idx, d_req_ids, pool->d_ctx,
-            pool->cfg.max_requests, T, H, K, sm_scale, o, d_lse);
-    else
-        decode_rowwise_kernel<false><<<grid, SIMPLE_WARPS * 32, 0, s>>>(
-            q, g, nullptr, d_resolved, d_topk_idx, d_req_ids, pool->d_ctx, pool->cfg.max_requests,
-            T, H, K, sm_scale, o, d_lse);
-    return cudaGetLastError() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+
+    CUtensorMap tq, tk;
+    if (!make_map(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_q, hs::kDim, pl.M, B, 2 * hs::kDim, 64,
+                  BM, CU_TENSOR_MAP_SWIZZLE_128B))
+        return HS_ERR_CUDA;
+    const bool ok_k =
+        fp8 ? make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, d_gathered, hs::kDim, K, B, hs::kDim, 64,
+                       BN, CU_TENSOR_MAP_SWIZZLE_NONE)
+            : make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_gathered, hs::kDim, K, B,
+                       2 * hs::kDim, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!ok_k) return HS_ERR_CUDA;
+
+    DecParams p{};
+    p.resolved = d_resolved;
+    p.topk = d_topk_idx;
+    p.req_ids = d_req_ids;
+    p.ctx = pool->d_ctx;
+    p.gscale = d_gathered_scale;
+    p.out = static_cast<__nv_bfloat16 *>(d_out);
+    p.lse = d_lse;
+    p.ws_o = pl.nsplit > 1 ? static_cast<float *>(d_workspace) : nullptr;
+    p.ws_lse = pl.nsplit > 1
+                   ? reinterpret_cast<float *>(static_cast<uint8_t *>(d_workspace) + pl.ws_o_bytes)
+                   : nullptr;
+    p.err = pool->d_err;
+    p.B = B;
+    p.T = T;
+    p.H = H;
+    p.K = K;
+    p.M = pl.M;
+    p.nsplit = pl.nsplit;
+    p.kps = pl.kps;
+    p.max_req = pool->cfg.max_requests;
+    p.scale_log2 = sm_scale * 1.4426950408889634f;
+
+    const dim3 grid(2 * pl.nsplit, pl.mtiles, B);
+    hs_status st;
+    if (fp8) {
+        if ((st = prepare_kernel<true>()) != HS_OK) return st;
+        decode_tc_kernel<true><<<grid, NTHR, Cfg<true>::SMEM_ALLOC, s>>>(tq, tk, p);
+    } else {
+        if ((st = prepare_kernel<false>()) != HS_OK) return st;
+        decode_tc_kernel<false><<<grid, NTHR, Cfg<false>::SMEM_ALLOC, s>>>(tq, tk, p);
+    }
+    if (cudaGetLastError() != cudaSuccess) return HS_ERR_CUDA;
+    if (pl.nsplit > 1) {
+        const int rows = B * pl.M;
+        combine_kernel<<<(rows + 7) / 8, 256, 0, s>>>(p.ws_o, p.ws_lse, pl.nsplit, rows, p.out, d_lse);
+        if (cudaGetLastError() != cudaSuccess) return HS_ERR_CUDA;
+    }
+    return HS_OK;
 }
