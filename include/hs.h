@@ -179,6 +179,31 @@ hs_status hs_sparse_mla_decode(hs_pool_t pool, int32_t B, int32_t T, int32_t H, 
                                size_t ws_bytes, void *stream);
 size_t hs_decode_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t K);
 
+/* hs_sparse_mla_decode without a caller-provided workspace. This entry point
+ * has no counterpart in the pages; it exists for callers that cannot allocate
+ * device memory: a host engine that has reserved the device's memory for its
+ * own KV pool and passes this library only tensors it already owns, or a C
+ * plugin that receives device pointers but has no allocator to call.
+ * The split-KV partials go to one array of HS_STATIC_DECODE_WS_BYTES bytes
+ * that lives in this library's device memory; every GPU that loads the
+ * library holds it until the process exits. The function itself allocates
+ * nothing. Arguments, layouts and results are those of hs_sparse_mla_decode.
+ *  - Shapes whose workspace (hs_decode_workspace_bytes) exceeds
+ *    HS_STATIC_DECODE_WS_BYTES return HS_ERR_CAPACITY and launch nothing.
+ *  - The first call on a device looks up that device's address of the array
+ *    (with that device current); make that first call before any stream
+ *    capture on the device.
+ *  - All calls share the one array and it keeps the last call's contents;
+ *    each call writes every entry it later reads, so nothing needs clearing.
+ *    Calls whose kernels overlap on the GPU (different streams without
+ *    ordering) race on the array: order them on one stream. */
+#define HS_STATIC_DECODE_WS_BYTES (24u << 20)
+hs_status hs_sparse_mla_decode_static_ws(hs_pool_t pool, int32_t B, int32_t T, int32_t H,
+                                         int32_t K, const void *d_q, const void *d_gathered,
+                                         const float *d_gathered_scale, const int32_t *d_resolved,
+                                         const int32_t *d_topk_idx, const int32_t *d_req_ids,
+                                         float sm_scale, void *d_out, float *d_lse, void *stream);
+
 /* Human-readable name of a status. */
 const char *hs_status_string(hs_status s);
 

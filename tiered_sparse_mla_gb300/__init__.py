@@ -31,8 +31,9 @@ EXPORTED = [
     "hs_page_map_range", "hs_hot_lease", "hs_hot_release", "hs_gpu_rows", "hs_host_rows",
     "hs_gpu_scales", "hs_host_scales", "hs_pool_snapshot", "hs_pool_restore",
     "hs_pool_get_error", "hs_resolve_topk", "hs_sparse_mla_decode",
-    "hs_decode_workspace_bytes", "hs_status_string",
+    "hs_decode_workspace_bytes", "hs_status_string", "hs_sparse_mla_decode_static_ws",
 ]
+HS_STATIC_DECODE_WS_BYTES = 24 << 20
 
 
 class HsError(RuntimeError):
@@ -90,6 +91,8 @@ def load() -> C.CDLL:
         "hs_sparse_mla_decode": ([vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, C.c_float,
                                   vp, vp, vp, sz, vp], i32),
         "hs_decode_workspace_bytes": ([i32, i32, i32, i32], sz),
+        "hs_sparse_mla_decode_static_ws": ([vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp,
+                                            C.c_float, vp, vp, vp], i32),
         "hs_status_string": ([i32], C.c_char_p),
     }
     for name, (args, res) in sig.items():
@@ -175,6 +178,18 @@ def hs_sparse_mla_decode(pool: int, q, gathered, gathered_scale, resolved, topk_
         pool, B, T, H, K, _ptr(q), _ptr(gathered), _ptr(gathered_scale), _ptr(resolved),
         _ptr(topk_idx), _ptr(req_ids), float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace),
         ws, _stream(stream)))
+
+
+def hs_sparse_mla_decode_static_ws(pool: int, q, gathered, gathered_scale, resolved, topk_idx,
+                                   req_ids, sm_scale: float, out, lse, stream=None):
+    """hs_sparse_mla_decode without a workspace argument, for callers that cannot
+    allocate device memory: the split-KV partials use a fixed array inside the
+    library (HS_STATIC_DECODE_WS_BYTES; see hs.h for the sharing rules)."""
+    B, T, H, _ = q.shape
+    K = topk_idx.shape[1]
+    _check("hs_sparse_mla_decode_static_ws", load().hs_sparse_mla_decode_static_ws(
+        pool, B, T, H, K, _ptr(q), _ptr(gathered), _ptr(gathered_scale), _ptr(resolved),
+        _ptr(topk_idx), _ptr(req_ids), float(sm_scale), _ptr(out), _ptr(lse), _stream(stream)))
 
 
 # ------------------------------------------------------------- convenience

@@ -727,3 +727,40 @@ extern "C" hs_status hs_sparse_mla_decode(hs_pool_t pool, int32_t B, int32_t T, 
     }
     return HS_OK;
 }
+
+// ---------------------------------------------------------------- no-allocation variant
+// Decode for callers that cannot allocate device memory themselves: a host
+// engine that has reserved the device's memory for its own KV pool and hands
+// this library only the tensors it owns, or a C plugin that receives device
+// pointers but has no allocator. The split-KV partials live in a fixed array in
+// this module's device memory instead of a caller-provided workspace. Every
+// GPU that loads the library holds the array until the process exits.
+static __device__ __align__(256) unsigned char hs_static_decode_ws[HS_STATIC_DECODE_WS_BYTES];
+
+namespace {
+void *g_static_ws[64];  // device address of hs_static_decode_ws, looked up once per device
+}
+
+extern "C" hs_status hs_sparse_mla_decode_static_ws(
+    hs_pool_t pool, int32_t B, int32_t T, int32_t H, int32_t K, const void *d_q,
+    const void *d_gathered, const float *d_gathered_scale, const int32_t *d_resolved,
+    const int32_t *d_topk_idx, const int32_t *d_req_ids, float sm_scale, void *d_out, float *d_lse,
+    void *stream) {
+    if (!pool || B < 0 || T < 1 || H < 1 || K < 1) return HS_ERR_INVALID_ARG;
+    if (B > 0 && hs_decode_workspace_bytes(B, T, H, K) > HS_STATIC_DECODE_WS_BYTES)
+        return HS_ERR_CAPACITY;
+    int dev = 0;
+    HS_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return HS_ERR_UNSUPPORTED;
+    if (!g_static_ws[dev]) {
+        // host code cannot use the array's name as a device address: ask the
+        // runtime for this device's copy (the current device)
+        void *p = nullptr;
+        HS_CUDA_TRY(cudaGetSymbolAddress(&p, hs_static_decode_ws));
+        if (!p) return HS_ERR_CUDA;
+        g_static_ws[dev] = p;
+    }
+    return hs_sparse_mla_decode(pool, B, T, H, K, d_q, d_gathered, d_gathered_scale, d_resolved,
+                                d_topk_idx, d_req_ids, sm_scale, d_out, d_lse, g_static_ws[dev],
+                                HS_STATIC_DECODE_WS_BYTES, stream);
+}
