@@ -9,24 +9,32 @@
 // position is <= that (MTP draft tokens share one top-K list, 与 vLLM 栈的集成).
 //
 // All H*T query rows of a request share the same K rows, so QK^T and PV are
-// dense contractions: S[128 x 64] = Q[128 x 576] K^T, O[128 x 256] += P V.
+// dense contractions: S[128 x 64] = Q[128 x 576] K^T, O[128 x 512] = P V.
 //
-// CTA = (request, 128-row M tile, 256-column half of the output, KV split).
-//   warp 0   TMA producer: Q once (9 boxes of 64 columns, 128B swizzle), then
-//            64-key x 64-column chunks of the gathered rows through a ring
-//            (BF16: straight into the ring; FP8: into a staging ring);
-//   warps 2-3 (FP8 only) convert e4m3 chunks to f16 with the row scale
-//            folded in, and Q from bf16 to f16 once;
-//   warp 1   MMA issuer (one thread): S_i = Q K_i^T into one of two TMEM S
-//            buffers, then O += P_i V_i. V is the same smem chunk as K, read
-//            through an MN-major descriptor, so no transpose is stored;
-//   warps 4-7 softmax, one thread per query row (TMEM lane): masking, online
-//            softmax with a conditional rescale (the running max only moves
-//            when a tile's max exceeds it by 2^8, so O in TMEM is rarely
-//            touched), P to smem, epilogue.
-// TMEM: O half 256 columns + 2 x 64 S columns (512 allocated). A full 512-wide
-// O would leave no TMEM for S, so the two output halves run in two CTAs that
-// both compute S (576-deep); the gathered rows are read from L2 twice.
+// Work unit: (request, 128-row M tile, KV split), run by a cluster of two CTAs.
+// The 576-wide rows are nine 64-column chunks. CTA h (h = 0, 1):
+//   - holds Q for its share of the QK depth (chunks 0-4 for h = 0, 5-8 for
+//     h = 1) and accumulates O for output columns [256h, 256h + 256) (V chunks
+//     0-3 or 4-7); per 64-key tile it therefore loads only chunks 4h..4h+4;
+//   - computes a partial S over its depth share into TMEM, sends it to the
+//     peer through distributed shared memory and adds the peer's partial, so
+//     both CTAs hold the same full S (fp32 addition is commutative, so the two
+//     sums are bit-identical) and take identical softmax decisions;
+//   - runs O_h += P V_h on its own V chunks.
+// Roles inside a CTA (256 threads):
+//   warp 0     TMA producer: Q once, then one 5-chunk tile group per 64 keys,
+//              double-buffered; L2 prefetch of the split's rows at start;
+//   warp 1     MMA issuer (one thread): S_i into one of two TMEM S buffers,
+//              then O += P_{i-1} V_{i-1}; V is read from the same smem chunks
+//              as K through an MN-major descriptor (no transpose stored);
+//   warps 2-3  FP8 only: convert e4m3 chunks in place to f16 with the row
+//              scale folded in, and Q from bf16 to f16 once;
+//   warps 4-7  one thread per query row (TMEM lane): stage the partial S,
+//              send it to the peer in one bulk shared-to-shared copy, add the
+//              peer's partial, masking, online softmax with a conditional
+//              rescale (the running max only moves when a tile's max exceeds
+//              it by 2^8), P to smem (over the sent staging), epilogue.
+// TMEM: O half 256 columns + 2 x 64 S columns (512 allocated).
 // Every mbarrier wait is bounded in time; on expiry the kernel sets
 // HS_DEVERR_TIMEOUT, drains its own copies and MMAs and returns.
 #include <cuda.h>
@@ -45,43 +53,45 @@ namespace {
 using namespace hs::tc;
 
 constexpr int NTHR = 256;
-constexpr int BM = 128, BN = 64, NCH = 9, NVC = 4;
+constexpr int BM = 128, BN = 64;
+constexpr int NLC = 5;               // chunks a CTA loads per 64-key tile
+constexpr int NG = 2;                // tile groups in flight
 constexpr int QCH_BYTES = BM * 128;  // 128 rows x 64 columns x 2 B
 constexpr int KCH_BYTES = BN * 128;  // 64 keys x 64 columns x 2 B
 constexpr int FCH_BYTES = BN * 64;   // 64 keys x 64 e4m3 codes
 constexpr int P_BYTES = BM * 128;    // 128 rows x 64 keys x 2 B
+constexpr int X_BYTES = BM * 256;    // 128 rows x 64 fp32 partial scores
 constexpr float TAU2 = 8.f;          // rescale threshold, log2 units
 constexpr uint32_t TMEM_COLS = 512, TM_O = 0, TM_S = 256;
 
-template <bool FP8>
 struct Cfg {
-    static constexpr int RING = FP8 ? 5 : 6;
-    static constexpr int FRING = FP8 ? 4 : 0;
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_RING = OFF_Q + NCH * QCH_BYTES;
-    static constexpr int OFF_P = OFF_RING + RING * KCH_BYTES;
-    static constexpr int OFF_F = OFF_P + P_BYTES;
-    static constexpr int OFF_BAR = OFF_F + FRING * FCH_BYTES;
-    static constexpr int B_QFULL = 0, B_QREADY = 1, B_DRAIN = 2, B_RFULL = 3;
-    static constexpr int B_REMPTY = B_RFULL + RING, B_SFULL = B_REMPTY + RING;
-    static constexpr int B_PFULL = B_SFULL + 2, B_PVDONE = B_PFULL + 1;
-    static constexpr int B_FFULL = B_PVDONE + 1, B_FEMPTY = B_FFULL + FRING;
-    static constexpr int NBAR = B_FEMPTY + FRING;
+    static constexpr int OFF_RING = OFF_Q + NLC * QCH_BYTES;
+    static constexpr int OFF_XIN = OFF_RING + NG * NLC * KCH_BYTES;  // the peer's partial S
+    static constexpr int OFF_XOUT = OFF_XIN + X_BYTES;  // own partial S, then P (same bytes)
+    static constexpr int OFF_P = OFF_XOUT;
+    static constexpr int OFF_KPOS = OFF_XOUT + X_BYTES;  // int32 [2][64]
+    static constexpr int OFF_BAR = OFF_KPOS + 2 * BN * 4;
+    static constexpr int B_QFULL = 0, B_QREADY = 1, B_DRAIN = 2, B_GFULL = 3;
+    static constexpr int B_GEMPTY = B_GFULL + NG, B_GLANDED = B_GEMPTY + NG;
+    static constexpr int B_SFULL = B_GLANDED + NG, B_PFULL = B_SFULL + 2;
+    static constexpr int B_PVDONE = B_PFULL + 1, B_XFULL = B_PVDONE + 1, B_XTAKEN = B_XFULL + 1;
+    static constexpr int NBAR = B_XTAKEN + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // [0] TMEM base, [1] abort flag
-    static constexpr int OFF_KPOS = OFF_MISC + 16;       // int32 [2][64]
-    static constexpr int SMEM = OFF_KPOS + 2 * BN * 4;
+    static constexpr int SMEM = OFF_MISC + 16;
     static constexpr int SMEM_ALLOC = SMEM + 1024;       // room to align the base to 1 KiB
-    static_assert(OFF_RING % 1024 == 0 && OFF_P % 1024 == 0 && OFF_F % 1024 == 0, "align");
+    static_assert(OFF_RING % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles need 1 KiB alignment");
     static_assert(SMEM_ALLOC <= 232448, "shared memory");
 };
 
 struct DecParams {
     const int32_t *resolved, *topk, *req_ids, *ctx;
     const float *gscale;
+    const uint8_t *gathered;
     __nv_bfloat16 *out;
     float *lse, *ws_o, *ws_lse;
     uint32_t *err;
-    int B, T, H, K, M, nsplit, kps, max_req;
+    int B, T, H, K, M, nsplit, kps, max_req, row_bytes;
     float scale_log2;
 };
 
@@ -152,40 +162,34 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// The chunk sequence shared by producer, converters and MMA issuer:
-// QK chunks of tile i (9), then the PV chunks of tile i-1 (the 4 V chunks of
-// this CTA's output half). `f(tile, chunk)` returns false to stop.
-template <typename F>
-__device__ __forceinline__ bool for_each_chunk(int ntiles, int half, F &&f) {
-    for (int i = 0; i <= ntiles; ++i) {
-        if (i < ntiles)
-            for (int c = 0; c < NCH; ++c)
-                if (!f(i, c)) return false;
-        if (i >= 1)
-            for (int c = half * NVC; c < half * NVC + NVC; ++c)
-                if (!f(i - 1, c)) return false;
-    }
-    return true;
+// Row r, 16-byte chunk c of the S exchange buffer (XOR swizzle against bank conflicts).
+__device__ __forceinline__ uint32_t x_off(int r, int c) {
+    return (uint32_t)(r * 256 + ((c ^ (r & 15)) << 4));
 }
 
 template <bool FP8>
 __global__ void __launch_bounds__(NTHR, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const DecParams p) {
-    using C = Cfg<FP8>;
+    using C = Cfg;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = hs::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (base - raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int half = blockIdx.x & 1, split = blockIdx.x >> 1, mt = blockIdx.y, b = blockIdx.z;
+    const int half = static_cast<int>(hs::cluster_ctarank());
+    const uint32_t peer = static_cast<uint32_t>(half ^ 1);
+    const int split = blockIdx.x >> 1, mt = blockIdx.y, b = blockIdx.z;
     const int k0 = split * p.kps, k1 = min(p.K, k0 + p.kps);
     const int ntiles = (k1 - k0 + BN - 1) / BN;
+    const int nq = half ? 4 : 5;      // Q chunks held (global chunks 5h .. 5h+nq-1)
+    const int lc0 = half ? 1 : 0;     // first local chunk used by QK (local chunk lc = global 4h+lc)
     volatile int32_t *misc = reinterpret_cast<volatile int32_t *>(smem + C::OFF_MISC);
     int32_t *kpos = reinterpret_cast<int32_t *>(smem + C::OFF_KPOS);
     const uint32_t sQ = base + C::OFF_Q, sR = base + C::OFF_RING, sP = base + C::OFF_P;
-    const uint32_t sF = base + C::OFF_F;
+    const uint32_t sXin = base + C::OFF_XIN, sXout = base + C::OFF_XOUT;
     auto bar = [&](int i) { return base + C::OFF_BAR + 8u * (uint32_t)i; };
+    auto slot = [&](int g, int lc) { return sR + (uint32_t)((g * NLC + lc) * KCH_BYTES); };
     auto fail = [&]() {
         misc[1] = 1;
         atomicOr(p.err, HS_DEVERR_TIMEOUT);
@@ -195,18 +199,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         mbar_init(bar(C::B_QFULL), 1);
         mbar_init(bar(C::B_QREADY), 64);
         mbar_init(bar(C::B_DRAIN), 1);
-        for (int i = 0; i < C::RING; ++i) {
-            mbar_init(bar(C::B_RFULL + i), FP8 ? 64 : 1);
-            mbar_init(bar(C::B_REMPTY + i), 1);
+        for (int g = 0; g < NG; ++g) {
+            mbar_init(bar(C::B_GFULL + g), FP8 ? 64 : 1);
+            mbar_init(bar(C::B_GEMPTY + g), 1);
+            mbar_init(bar(C::B_GLANDED + g), 1);
         }
         mbar_init(bar(C::B_SFULL), 1);
         mbar_init(bar(C::B_SFULL + 1), 1);
         mbar_init(bar(C::B_PFULL), 128);
         mbar_init(bar(C::B_PVDONE), 1);
-        for (int i = 0; i < C::FRING; ++i) {
-            mbar_init(bar(C::B_FFULL + i), 1);
-            mbar_init(bar(C::B_FEMPTY + i), 64);
-        }
+        mbar_init(bar(C::B_XFULL), 1);   // own arm + the peer's bulk copy bytes
+        mbar_init(bar(C::B_XTAKEN), 1);  // the peer has read what this CTA sent
         misc[1] = 0;
         fence_mbar_init();
     }
@@ -218,41 +221,45 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    cluster_sync_all();  // the peer's barriers are initialised before any remote arrive
     const uint32_t tmem = static_cast<uint32_t>(misc[0]);
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            mbar_expect_tx(bar(C::B_QFULL), NCH * QCH_BYTES);
-            for (int c = 0; c < NCH; ++c)
-                tma_load_3d(sQ + c * QCH_BYTES, &tm_q, 64 * c, mt * BM, b, bar(C::B_QFULL));
-            constexpr int NS = FP8 ? C::FRING : C::RING;
-            int slot = 0, issued = 0;
-            uint32_t ph = 0;
-            const bool ok = for_each_chunk(ntiles, half, [&](int tile, int c) {
-                const uint32_t empty = bar((FP8 ? C::B_FEMPTY : C::B_REMPTY) + slot);
-                const uint32_t full = bar((FP8 ? C::B_FFULL : C::B_RFULL) + slot);
-                if (!mbar_wait(empty, ph ^ 1) || misc[1]) return false;
-                if (FP8) {
-                    mbar_expect_tx(full, FCH_BYTES);
-                    tma_load_3d(sF + slot * FCH_BYTES, &tm_k, 64 * c, k0 + tile * BN, b, full);
-                } else {
-                    mbar_expect_tx(full, KCH_BYTES);
-                    tma_load_3d(sR + slot * KCH_BYTES, &tm_k, 64 * c, k0 + tile * BN, b, full);
+            mbar_expect_tx(bar(C::B_QFULL), nq * QCH_BYTES);
+            for (int c = 0; c < nq; ++c)
+                tma_load_3d(sQ + c * QCH_BYTES, &tm_q, 64 * (5 * half + c), mt * BM, b,
+                            bar(C::B_QFULL));
+            if (half == 0) {  // stream this split's rows into L2 ahead of the tile loads
+                for (int i = 0; i < ntiles; ++i) {
+                    const int j = k0 + i * BN, n = min(BN, k1 - j);
+                    prefetch_l2(p.gathered + ((size_t)b * p.K + j) * p.row_bytes,
+                                (uint32_t)(n * p.row_bytes));
                 }
+            }
+            int issued = 0;
+            bool ok = true;
+            for (int i = 0; i < ntiles && ok; ++i) {
+                const int g = i % NG;
+                const uint32_t ph = (uint32_t)(i / NG) & 1u;
+                if (!mbar_wait(bar(C::B_GEMPTY + g), ph ^ 1u) || misc[1]) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t done = bar((FP8 ? C::B_GLANDED : C::B_GFULL) + g);
+                mbar_expect_tx(done, NLC * (FP8 ? FCH_BYTES : KCH_BYTES));
+                for (int lc = 0; lc < NLC; ++lc)
+                    tma_load_3d(slot(g, lc) + (FP8 ? KCH_BYTES - FCH_BYTES : 0), &tm_k,
+                                64 * (4 * half + lc), k0 + i * BN, b, done);
                 ++issued;
-                if (++slot == NS) {
-                    slot = 0;
-                    ph ^= 1;
-                }
-                return true;
-            });
+            }
             if (!ok) {
                 fail();
                 // let the copies this thread started land before the CTA exits
                 mbar_wait(bar(C::B_QFULL), 0);
-                for (int k = issued - 1; k >= 0 && k >= issued - NS; --k)
-                    mbar_wait(bar((FP8 ? C::B_FFULL : C::B_RFULL) + k % NS), (k / NS) & 1);
+                for (int i = issued - 1; i >= 0 && i >= issued - NG; --i)
+                    mbar_wait(bar((FP8 ? C::B_GLANDED : C::B_GFULL) + i % NG), (i / NG) & 1);
             }
         }
     } else if (warp == 1) {
@@ -260,61 +267,43 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (lane == 0) {
             constexpr uint32_t AB = FP8 ? 0u : 1u;
             constexpr uint32_t ID_QK = idesc_f16(AB, 0, BM, BN);
-            constexpr uint32_t ID_PV = idesc_f16(AB, 1, BM, BN);
+            constexpr uint32_t ID_PV = idesc_f16(AB, 1, BM, 256);
             bool ok = mbar_wait(bar(FP8 ? C::B_QREADY : C::B_QFULL), 0);
             tc_fence_after();
-            int slot = 0;
-            uint32_t ph = 0;
             for (int i = 0; i <= ntiles && ok; ++i) {
                 if (i < ntiles) {
-                    const uint32_t dS = tmem + TM_S + (uint32_t)(i & 1) * BN;
-                    for (int c = 0; c < NCH && ok; ++c) {
-                        if (!mbar_wait(bar(C::B_RFULL + slot), ph)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint64_t a = desc_sw128(sQ + c * QCH_BYTES + k * 32, 16, 1024);
-                            const uint64_t bd = desc_sw128(sR + slot * KCH_BYTES + k * 32, 16, 1024);
-                            mma_f16(dS, a, bd, ID_QK, (c | k) != 0);
-                        }
-                        mma_commit(bar(C::B_REMPTY + slot));
-                        if (++slot == C::RING) {
-                            slot = 0;
-                            ph ^= 1;
-                        }
-                    }
-                    if (!ok) break;
-                    mma_commit(bar(C::B_SFULL + (i & 1)));
-                }
-                if (i >= 1) {
-                    if (!mbar_wait(bar(C::B_PFULL), (i - 1) & 1)) {
+                    const int g = i % NG;
+                    if (!mbar_wait(bar(C::B_GFULL + g), (uint32_t)(i / NG) & 1u)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    for (int c = 0; c < NVC && ok; ++c) {
-                        if (!mbar_wait(bar(C::B_RFULL + slot), ph)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
+                    const uint32_t dS = tmem + TM_S + (uint32_t)(i & 1) * BN;
+                    for (int lc = lc0; lc < NLC; ++lc) {
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t a = desc_sw128(sP + kk * 32, 16, 1024);
-                            const uint64_t bd =
-                                desc_sw128(sR + slot * KCH_BYTES + kk * 2048, KCH_BYTES, 1024);
-                            mma_f16(tmem + TM_O + 64 * c, a, bd, ID_PV, (i > 1) || (kk > 0));
-                        }
-                        mma_commit(bar(C::B_REMPTY + slot));
-                        if (++slot == C::RING) {
-                            slot = 0;
-                            ph ^= 1;
+                        for (int k = 0; k < 4; ++k) {
+                            const uint64_t a =
+                                desc_sw128(sQ + (lc - lc0) * QCH_BYTES + k * 32, 16, 1024);
+                            const uint64_t bd = desc_sw128(slot(g, lc) + k * 32, 16, 1024);
+                            mma_f16(dS, a, bd, ID_QK, (lc > lc0) || (k > 0));
                         }
                     }
-                    if (!ok) break;
+                    mma_commit(bar(C::B_SFULL + (i & 1)));
+                }
+                if (i >= 1) {
+                    const int j = i - 1, g = j % NG;
+                    if (!mbar_wait(bar(C::B_PFULL), (uint32_t)j & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {  // O[128 x 256] += P[:, 16kk..] V[16kk.., 0..256)
+                        const uint64_t a = desc_sw128(sP + kk * 32, 16, 1024);
+                        const uint64_t bd = desc_sw128(slot(g, 0) + kk * 2048, KCH_BYTES, 1024);
+                        mma_f16(tmem + TM_O, a, bd, ID_PV, (j > 0) || (kk > 0));
+                    }
+                    mma_commit(bar(C::B_GEMPTY + g));
                     mma_commit(bar(C::B_PVDONE));
                 }
                 if (misc[1]) ok = false;
@@ -327,10 +316,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     } else if (warp < 4) {
         // ------------------------------------------------------------ FP8 converters
         if (FP8) {
-            const int ct = threadIdx.x - 64;  // 0..63: one key row per chunk
+            const int ct = threadIdx.x - 64;  // 0..63: one key row of every chunk
             bool ok = mbar_wait(bar(C::B_QFULL), 0);
             if (ok) {
-                for (int q = ct; q < NCH * QCH_BYTES / 16; q += 64) {
+                for (int q = ct; q < nq * QCH_BYTES / 16; q += 64) {
                     const uint4 v = ld_shared_v4(sQ + q * 16);
                     st_shared_v4(sQ + q * 16, bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y),
                                  bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
@@ -340,49 +329,43 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 fail();
             }
             mbar_arrive(bar(C::B_QREADY));
-            int fslot = 0, slot = 0, cur_tile = -1;
-            uint32_t fph = 0, ph = 0;
-            __half2 s2 = __float2half2_rn(0.f);
             const float *gs = p.gscale + (size_t)b * p.K;
-            ok = ok && for_each_chunk(ntiles, half, [&](int tile, int c) {
-                if (tile != cur_tile) {
-                    cur_tile = tile;
-                    const int j = k0 + tile * BN + ct;
-                    s2 = __float2half2_rn(j < p.K ? gs[j] : 0.f);
-                }
-                if (!mbar_wait(bar(C::B_FFULL + fslot), fph) || misc[1]) return false;
-                const uint32_t src = sF + fslot * FCH_BYTES + ct * 64;
-                uint4 raw4[4];
+            for (int i = 0; i < ntiles; ++i) {
+                const int g = i % NG;
+                if (ok) ok = mbar_wait(bar(C::B_GLANDED + g), (uint32_t)(i / NG) & 1u) && !misc[1];
+                const int j = k0 + i * BN + ct;
+                const __half2 s2 = __float2half2_rn(j < p.K ? gs[j] : 0.f);
+                for (int lc = 0; lc < NLC; ++lc) {
+                    // the e4m3 codes sit in the upper half of the slot; every row
+                    // is read before any f16 row (which may overlap them) is written
+                    const uint32_t sl = slot(g, lc);
+                    uint4 raw4[4];
+                    if (ok) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) raw4[q] = ld_shared_v4(src + 16 * q);
-                mbar_arrive(bar(C::B_FEMPTY + fslot));
-                if (++fslot == C::FRING) {
-                    fslot = 0;
-                    fph ^= 1;
-                }
-                if (!mbar_wait(bar(C::B_REMPTY + slot), ph ^ 1)) return false;
-                const uint32_t dst = sR + slot * KCH_BYTES + ct * 128;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {  // 16 codes -> 16 f16 = two 16-byte chunks
-                    const uint32_t w[4] = {raw4[q].x, raw4[q].y, raw4[q].z, raw4[q].w};
-                    uint32_t h[8];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        h[2 * e] = hmul2_u32(e4m3x2_to_f16x2(w[e] & 0xffffu), s2);
-                        h[2 * e + 1] = hmul2_u32(e4m3x2_to_f16x2(w[e] >> 16), s2);
+                        for (int q = 0; q < 4; ++q)
+                            raw4[q] = ld_shared_v4(sl + (KCH_BYTES - FCH_BYTES) + ct * 64 + 16 * q);
                     }
-                    const int c0 = 2 * q, c1 = 2 * q + 1;
-                    st_shared_v4(dst + ((c0 ^ (ct & 7)) << 4), h[0], h[1], h[2], h[3]);
-                    st_shared_v4(dst + ((c1 ^ (ct & 7)) << 4), h[4], h[5], h[6], h[7]);
+                    named_bar_sync(2, 64);
+                    if (!ok) continue;
+                    const uint32_t dst = sl + ct * 128;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {  // 16 codes -> 16 f16 = two 16-byte chunks
+                        const uint32_t w[4] = {raw4[q].x, raw4[q].y, raw4[q].z, raw4[q].w};
+                        uint32_t h[8];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            h[2 * e] = hmul2_u32(e4m3x2_to_f16x2(w[e] & 0xffffu), s2);
+                            h[2 * e + 1] = hmul2_u32(e4m3x2_to_f16x2(w[e] >> 16), s2);
+                        }
+                        st_shared_v4(dst + (((2 * q) ^ (ct & 7)) << 4), h[0], h[1], h[2], h[3]);
+                        st_shared_v4(dst + (((2 * q + 1) ^ (ct & 7)) << 4), h[4], h[5], h[6], h[7]);
+                    }
                 }
-                fence_proxy_async();
-                mbar_arrive(bar(C::B_RFULL + slot));
-                if (++slot == C::RING) {
-                    slot = 0;
-                    ph ^= 1;
+                if (ok) {
+                    fence_proxy_async();
+                    mbar_arrive(bar(C::B_GFULL + g));
                 }
-                return true;
-            });
+            }
             if (!ok) fail();
         }
     } else {
@@ -398,85 +381,123 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const int pos = L - p.T + t;
         const int32_t *res_b = p.resolved + (size_t)b * p.K;
         const int32_t *top_b = p.topk + (size_t)b * p.K;
+        // position of key `idx` of this split; INT_MAX for unresolved or absent entries
+        auto key_pos = [&](int idx) {
+            const int j = k0 + idx;
+            return (j < k1 && res_b[j] >= 0) ? top_b[j] : INT_MAX;
+        };
+        if (row < BN) kpos[row] = key_pos(row);
+        named_bar_sync(1, 128);
+        const uint32_t peer_xin = hs::dsmem_map(smem + C::OFF_XIN, peer);
+        const uint32_t peer_xfull = hs::dsmem_map(smem + C::OFF_BAR + 8 * C::B_XFULL, peer);
+        const uint32_t peer_xtaken = hs::dsmem_map(smem + C::OFF_BAR + 8 * C::B_XTAKEN, peer);
         float m2 = -INFINITY, l = 0.f;
         bool ok = true;
-        // every softmax thread runs all ntiles iterations (the named barrier is
-        // not bounded in time); after a failed wait the work is skipped
+        // Every softmax thread runs every iteration and reaches every named
+        // barrier (those are not bounded in time); after a failed wait the
+        // remaining work is skipped.
         for (int i = 0; i < ntiles; ++i) {
-            if (row < BN) {
-                const int j = k0 + i * BN + row;
-                int kp = INT_MAX;
-                if (j < k1 && res_b[j] >= 0) kp = top_b[j];
-                kpos[(i & 1) * BN + row] = kp;
+            const int kp_next = (row < BN && i + 1 < ntiles) ? key_pos((i + 1) * BN + row) : INT_MAX;
+            uint32_t ra[32], rb[32];
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SFULL + (i & 1)), (i >> 1) & 1));
+            if (ok && i > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_PVDONE), (i - 1) & 1));
+            if (ok) {
+                // own partial scores -> staging (X_out; P of the previous tile is consumed)
+                tc_fence_after();
+                const uint32_t tS = tmem + lane_off + TM_S + (uint32_t)(i & 1) * BN;
+                HS_TMEM_LD32(tS, ra);
+                HS_TMEM_LD32(tS + 32, rb);
+                HS_TMEM_WAIT_LD32(ra);
+                HS_TMEM_WAIT_LD32(rb);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const uint32_t *src = c < 8 ? &ra[4 * c] : &rb[4 * (c - 8)];
+                    st_shared_v4(sXout + x_off(row, c), src[0], src[1], src[2], src[3]);
+                }
+                fence_proxy_async();
             }
             named_bar_sync(1, 128);
-            if (!ok) continue;
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SFULL + (i & 1)), (i >> 1) & 1));
-            if (!ok) continue;
-            tc_fence_after();
-            uint32_t ra[32], rb[32];
-            const uint32_t tS = tmem + lane_off + TM_S + (uint32_t)(i & 1) * BN;
-            HS_TMEM_LD32(tS, ra);
-            HS_TMEM_LD32(tS + 32, rb);
-            HS_TMEM_WAIT_LD32(ra);
-            HS_TMEM_WAIT_LD32(rb);
+            if (row == 0 && ok) {
+                // arm own receive barrier, then send the 32 KiB partial in one bulk copy
+                mbar_expect_tx(bar(C::B_XFULL), X_BYTES);
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes"
+                    " [%0], [%1], %2, [%3];" ::"r"(peer_xin),
+                    "r"(sXout), "r"((uint32_t)X_BYTES), "r"(peer_xfull)
+                    : "memory");
+            }
             float s[64];
-            float tmax = -INFINITY;
-            const int32_t *kp = kpos + (i & 1) * BN;
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar(C::B_XFULL), i & 1));
+            if (ok) {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                const float raw_s = __uint_as_float(j < 32 ? ra[j] : rb[j - 32]);
-                const float v = kp[j] <= pos ? raw_s * p.scale_log2 : -INFINITY;
-                s[j] = v;
-                tmax = fmaxf(tmax, v);
-            }
-            if (i > 0) {
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_PVDONE), (i - 1) & 1));
-                if (!ok) continue;
-                tc_fence_after();
-            }
-            if (i == 0) {
-                m2 = tmax;
-            } else {
-                const bool need = tmax > m2 + TAU2;
-                if (__any_sync(0xffffffffu, need)) {
-                    const float alpha = need ? exp2f(m2 - tmax) : 1.f;
-                    if (need) {
-                        l *= alpha;
-                        m2 = tmax;
-                    }
-#pragma unroll 1
-                    for (int cc = 0; cc < 8; ++cc) {
-                        uint32_t o[32];
-                        const uint32_t tO = tmem + lane_off + TM_O + 32 * cc;
-                        HS_TMEM_LD32(tO, o);
-                        HS_TMEM_WAIT_LD32(o);
-                        float f[32];
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(o[e]) * alpha;
-                        tmem_st32(tO, f);
-                    }
-                    tmem_wait_st();
+                for (int c = 0; c < 16; ++c) {
+                    const uint4 v = ld_shared_v4(sXin + x_off(row, c));
+                    const uint32_t *own = c < 8 ? &ra[4 * c] : &rb[4 * (c - 8)];
+                    s[4 * c] = __uint_as_float(own[0]) + __uint_as_float(v.x);
+                    s[4 * c + 1] = __uint_as_float(own[1]) + __uint_as_float(v.y);
+                    s[4 * c + 2] = __uint_as_float(own[2]) + __uint_as_float(v.z);
+                    s[4 * c + 3] = __uint_as_float(own[3]) + __uint_as_float(v.w);
                 }
             }
-            const float mref = (m2 == -INFINITY) ? 0.f : m2;
-            float lsum = 0.f;
-            uint32_t pk[32];
+            named_bar_sync(1, 128);
+            if (row == 0 && ok) mbar_arrive_remote(peer_xtaken);  // X_in may be refilled
+            if (ok) {
+                float tmax = -INFINITY;
+                const int32_t *kp = kpos + (i & 1) * BN;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const float a = exp2f(s[2 * e] - mref), c = exp2f(s[2 * e + 1] - mref);
-                lsum += a + c;
-                pk[e] = pack2<FP8>(a, c);
+                for (int j = 0; j < 64; ++j) {
+                    const float v = kp[j] <= pos ? s[j] * p.scale_log2 : -INFINITY;
+                    s[j] = v;
+                    tmax = fmaxf(tmax, v);
+                }
+                if (i == 0) {
+                    m2 = tmax;
+                } else {
+                    const bool need = tmax > m2 + TAU2;
+                    if (__any_sync(0xffffffffu, need)) {
+                        const float alpha = need ? exp2f(m2 - tmax) : 1.f;
+                        if (need) {
+                            l *= alpha;
+                            m2 = tmax;
+                        }
+#pragma unroll 1
+                        for (int cc = 0; cc < 8; ++cc) {
+                            uint32_t o[32];
+                            const uint32_t tO = tmem + lane_off + TM_O + 32 * cc;
+                            HS_TMEM_LD32(tO, o);
+                            HS_TMEM_WAIT_LD32(o);
+                            float f[32];
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(o[e]) * alpha;
+                            tmem_st32(tO, f);
+                        }
+                        tmem_wait_st();
+                    }
+                }
+                const float mref = (m2 == -INFINITY) ? 0.f : m2;
+                float lsum = 0.f;
+                uint32_t pk[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float a = exp2f(s[2 * e] - mref), c = exp2f(s[2 * e + 1] - mref);
+                    lsum += a + c;
+                    pk[e] = pack2<FP8>(a, c);
+                }
+                l += lsum;
+                // P overwrites the staged partial once the peer has taken it
+                ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar(C::B_XTAKEN), i & 1));
+                if (ok) {
+                    const uint32_t prow = sP + row * 128;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        st_shared_v4(prow + ((q ^ (row & 7)) << 4), pk[4 * q], pk[4 * q + 1],
+                                     pk[4 * q + 2], pk[4 * q + 3]);
+                    fence_proxy_async();
+                    tc_fence_before();
+                    mbar_arrive(bar(C::B_PFULL));
+                }
             }
-            l += lsum;
-            const uint32_t prow = sP + row * 128;
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                st_shared_v4(prow + ((q ^ (row & 7)) << 4), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
-                             pk[4 * q + 3]);
-            fence_proxy_async();
-            tc_fence_before();
-            mbar_arrive(bar(C::B_PFULL));
+            if (row < BN && i + 1 < ntiles) kpos[((i + 1) & 1) * BN + row] = kp_next;
         }
         if (ok && ntiles > 0) {
             ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_PVDONE), (ntiles - 1) & 1));
@@ -529,6 +550,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+    cluster_sync_all();  // no CTA leaves while its peer may still write to it
 }
 
 // Merges the KV-split partials: out = sum_s w_s O_s / sum_s w_s, w_s = exp(lse_s - max).
@@ -639,15 +661,28 @@ bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, uint64_t 
 }
 
 template <bool FP8>
-hs_status prepare_kernel() {
-    static bool done = false;
-    if (!done) {
+hs_status launch_decode(dim3 grid, cudaStream_t s, const CUtensorMap &tq, const CUtensorMap &tk,
+                        const DecParams &p) {
+    static bool ready = false;
+    if (!ready) {
         HS_CUDA_TRY(cudaFuncSetAttribute(decode_tc_kernel<FP8>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<FP8>::SMEM_ALLOC));
-        done = true;
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_ALLOC));
+        ready = true;
     }
-    return HS_OK;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(NTHR, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_ALLOC;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;  // the two output halves of one work unit
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<FP8>, tq, tk, p) == cudaSuccess ? HS_OK
+                                                                                   : HS_ERR_CUDA;
 }
 
 }  // namespace
@@ -693,6 +728,8 @@ extern "C" hs_status hs_sparse_mla_decode(hs_pool_t pool, int32_t B, int32_t T, 
     p.req_ids = d_req_ids;
     p.ctx = pool->d_ctx;
     p.gscale = d_gathered_scale;
+    p.gathered = static_cast<const uint8_t *>(d_gathered);
+    p.row_bytes = fp8 ? hs::kDim : 2 * hs::kDim;
     p.out = static_cast<__nv_bfloat16 *>(d_out);
     p.lse = d_lse;
     p.ws_o = pl.nsplit > 1 ? static_cast<float *>(d_workspace) : nullptr;
@@ -711,15 +748,9 @@ extern "C" hs_status hs_sparse_mla_decode(hs_pool_t pool, int32_t B, int32_t T, 
     p.scale_log2 = sm_scale * 1.4426950408889634f;
 
     const dim3 grid(2 * pl.nsplit, pl.mtiles, B);
-    hs_status st;
-    if (fp8) {
-        if ((st = prepare_kernel<true>()) != HS_OK) return st;
-        decode_tc_kernel<true><<<grid, NTHR, Cfg<true>::SMEM_ALLOC, s>>>(tq, tk, p);
-    } else {
-        if ((st = prepare_kernel<false>()) != HS_OK) return st;
-        decode_tc_kernel<false><<<grid, NTHR, Cfg<false>::SMEM_ALLOC, s>>>(tq, tk, p);
-    }
-    if (cudaGetLastError() != cudaSuccess) return HS_ERR_CUDA;
+    const hs_status st = fp8 ? launch_decode<true>(grid, s, tq, tk, p)
+                             : launch_decode<false>(grid, s, tq, tk, p);
+    if (st != HS_OK) return st;
     if (pl.nsplit > 1) {
         const int rows = B * pl.M;
         combine_kernel<<<(rows + 7) / 8, 256, 0, s>>>(p.ws_o, p.ws_lse, pl.nsplit, rows, p.out, d_lse);
