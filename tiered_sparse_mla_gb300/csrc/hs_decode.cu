@@ -16,12 +16,13 @@
 //   - holds Q for its share of the QK depth (chunks 0-4 for h = 0, 5-8 for
 //     h = 1) and accumulates O for output columns [256h, 256h + 256) (V chunks
 //     0-3 or 4-7); per 64-key tile it therefore loads only chunks 4h..4h+4;
-//   - computes a partial S over its depth share into TMEM, sends it to the
-//     peer through distributed shared memory and adds the peer's partial, so
-//     both CTAs hold the same full S (fp32 addition is commutative, so the two
-//     sums are bit-identical) and take identical softmax decisions;
+//   - computes a partial S over its depth share into TMEM, sends it (rounded
+//     to f16 after scaling by sm_scale * log2 e) to the peer through
+//     distributed shared memory and adds the peer's partial; both CTAs add
+//     the same two rounded values, so they hold bit-identical S and take
+//     identical softmax decisions;
 //   - runs O_h += P V_h on its own V chunks.
-// Roles inside a CTA (256 threads):
+// Roles inside a CTA (288 threads):
 //   warp 0     TMA producer: Q once, then one 5-chunk tile group per 64 keys,
 //              double-buffered; L2 prefetch of the split's rows at start;
 //   warp 1     MMA issuer (one thread): S_i into one of two TMEM S buffers,
@@ -29,11 +30,14 @@
 //              as K through an MN-major descriptor (no transpose stored);
 //   warps 2-3  FP8 only: convert e4m3 chunks in place to f16 with the row
 //              scale folded in, and Q from bf16 to f16 once;
-//   warps 4-7  one thread per query row (TMEM lane): stage the partial S,
-//              send it to the peer in one bulk shared-to-shared copy, add the
-//              peer's partial, masking, online softmax with a conditional
-//              rescale (the running max only moves when a tile's max exceeds
-//              it by 2^8), P to smem (over the sent staging), epilogue.
+//   warps 4-7  one thread per query row (TMEM lane): stage the partial S as
+//              f16 of S * sm_scale * log2(e) (the next tile's partial while
+//              this tile's PV runs), add the peer's partial, masking, online
+//              softmax with a conditional rescale (the running max only moves
+//              when a tile's max exceeds it by 2^8), P to smem, epilogue;
+//   warp 8     courier: sends each staged partial to the peer in one bulk
+//              shared-to-shared copy and tells the peer when its partial has
+//              been read, so no softmax warp waits on a cluster-scope release.
 // TMEM: O half 256 columns + 2 x 64 S columns (512 allocated).
 // Every mbarrier wait is bounded in time; on expiry the kernel sets
 // HS_DEVERR_TIMEOUT, drains its own copies and MMAs and returns.
@@ -52,7 +56,7 @@ namespace {
 
 using namespace hs::tc;
 
-constexpr int NTHR = 256;
+constexpr int NTHR = 288;  // 9 warps
 constexpr int BM = 128, BN = 64;
 constexpr int NLC = 5;               // chunks a CTA loads per 64-key tile
 constexpr int NG = 2;                // tile groups in flight
@@ -60,16 +64,16 @@ constexpr int QCH_BYTES = BM * 128;  // 128 rows x 64 columns x 2 B
 constexpr int KCH_BYTES = BN * 128;  // 64 keys x 64 columns x 2 B
 constexpr int FCH_BYTES = BN * 64;   // 64 keys x 64 e4m3 codes
 constexpr int P_BYTES = BM * 128;    // 128 rows x 64 keys x 2 B
-constexpr int X_BYTES = BM * 256;    // 128 rows x 64 fp32 partial scores
+constexpr int X_BYTES = BM * 128;    // 128 rows x 64 f16 partial scores
 constexpr float TAU2 = 8.f;          // rescale threshold, log2 units
 constexpr uint32_t TMEM_COLS = 512, TM_O = 0, TM_S = 256;
 
 struct Cfg {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_RING = OFF_Q + NLC * QCH_BYTES;
-    static constexpr int OFF_XIN = OFF_RING + NG * NLC * KCH_BYTES;  // the peer's partial S
-    static constexpr int OFF_XOUT = OFF_XIN + X_BYTES;  // own partial S, then P (same bytes)
-    static constexpr int OFF_P = OFF_XOUT;
+    static constexpr int OFF_P = OFF_RING + NG * NLC * KCH_BYTES;
+    static constexpr int OFF_XIN = OFF_P + P_BYTES;      // the peer's partial S (f16)
+    static constexpr int OFF_XOUT = OFF_XIN + X_BYTES;   // own partial S (f16), sent to the peer
     static constexpr int OFF_KPOS = OFF_XOUT + X_BYTES;  // int32 [2][64]
     static constexpr int OFF_BAR = OFF_KPOS + 2 * BN * 4;
     static constexpr int B_QFULL = 0, B_QREADY = 1, B_DRAIN = 2, B_GFULL = 3;
@@ -162,9 +166,13 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Row r, 16-byte chunk c of the S exchange buffer (XOR swizzle against bank conflicts).
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t n) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Row r, 16-byte chunk c of an S exchange buffer (XOR swizzle against bank conflicts).
 __device__ __forceinline__ uint32_t x_off(int r, int c) {
-    return (uint32_t)(r * 256 + ((c ^ (r & 15)) << 4));
+    return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
 template <bool FP8>
@@ -345,7 +353,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         for (int q = 0; q < 4; ++q)
                             raw4[q] = ld_shared_v4(sl + (KCH_BYTES - FCH_BYTES) + ct * 64 + 16 * q);
                     }
-                    named_bar_sync(2, 64);
+                    named_bar_sync(4, 64);  // converter warps only (ids 1-3 belong to softmax + courier)
                     if (!ok) continue;
                     const uint32_t dst = sl + ct * 128;
 #pragma unroll
@@ -368,6 +376,37 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             if (!ok) fail();
         }
+    } else if (warp == 8) {
+        // ------------------------------------------------------------ courier
+        // Sends each staged partial to the peer and tells the peer when its
+        // data has been read, so that the softmax warps never wait on the
+        // release of a cluster-scope arrive. Mirrors the softmax loop's
+        // barrier sequence: staged(0), then per tile: read(i), staged(i+1).
+        const uint32_t peer_xin = hs::dsmem_map(smem + C::OFF_XIN, peer);
+        const uint32_t peer_xfull = hs::dsmem_map(smem + C::OFF_BAR + 8 * C::B_XFULL, peer);
+        const uint32_t peer_xtaken = hs::dsmem_map(smem + C::OFF_BAR + 8 * C::B_XTAKEN, peer);
+        auto send = [&]() {
+            if (lane == 0 && !misc[1]) {
+                mbar_expect_tx(bar(C::B_XFULL), X_BYTES);  // this CTA's next receive
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes"
+                    " [%0], [%1], %2, [%3];" ::"r"(peer_xin),
+                    "r"(sXout), "r"((uint32_t)X_BYTES), "r"(peer_xfull)
+                    : "memory");
+            }
+        };
+        if (ntiles > 0) {
+            named_bar_sync(3, 160);
+            send();
+        }
+        for (int i = 0; i < ntiles; ++i) {
+            named_bar_sync(2, 160);
+            if (lane == 0 && !misc[1]) mbar_arrive_remote(peer_xtaken);
+            if (i + 1 < ntiles) {
+                named_bar_sync(3, 160);
+                send();
+            }
+        }
     } else {
         // ------------------------------------------------------------ softmax + epilogue
         const int wq = warp - 4;
@@ -388,68 +427,83 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         };
         if (row < BN) kpos[row] = key_pos(row);
         named_bar_sync(1, 128);
-        const uint32_t peer_xin = hs::dsmem_map(smem + C::OFF_XIN, peer);
-        const uint32_t peer_xfull = hs::dsmem_map(smem + C::OFF_BAR + 8 * C::B_XFULL, peer);
-        const uint32_t peer_xtaken = hs::dsmem_map(smem + C::OFF_BAR + 8 * C::B_XTAKEN, peer);
         float m2 = -INFINITY, l = 0.f;
         bool ok = true;
-        // Every softmax thread runs every iteration and reaches every named
-        // barrier (those are not bounded in time); after a failed wait the
-        // remaining work is skipped.
-        for (int i = 0; i < ntiles; ++i) {
-            const int kp_next = (row < BN && i + 1 < ntiles) ? key_pos((i + 1) * BN + row) : INT_MAX;
-            uint32_t ra[32], rb[32];
+        // Partial scores travel as f16 of S * sm_scale * log2(e); both CTAs add
+        // the same two rounded values, so their sums are bit-identical.
+        uint32_t own[32];  // this CTA's partial for the tile being sent / processed
+        // Stage tile `i`: read the partial from TMEM, keep it packed, write it
+        // to X_out and (one thread) send it to the peer. Every thread of the
+        // softmax group calls this the same number of times (named barrier).
+        auto stage = [&](int i) {
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SFULL + (i & 1)), (i >> 1) & 1));
-            if (ok && i > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_PVDONE), (i - 1) & 1));
+            // X_out still holds tile i-1 until the peer has taken it
+            if (ok && i > 0)
+                ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar(C::B_XTAKEN), (i - 1) & 1));
             if (ok) {
-                // own partial scores -> staging (X_out; P of the previous tile is consumed)
                 tc_fence_after();
+                uint32_t ra[32], rb[32];
                 const uint32_t tS = tmem + lane_off + TM_S + (uint32_t)(i & 1) * BN;
                 HS_TMEM_LD32(tS, ra);
                 HS_TMEM_LD32(tS + 32, rb);
                 HS_TMEM_WAIT_LD32(ra);
                 HS_TMEM_WAIT_LD32(rb);
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const uint32_t *src = c < 8 ? &ra[4 * c] : &rb[4 * (c - 8)];
-                    st_shared_v4(sXout + x_off(row, c), src[0], src[1], src[2], src[3]);
+                for (int e = 0; e < 16; ++e) {
+                    own[e] = pack2<true>(__uint_as_float(ra[2 * e]) * p.scale_log2,
+                                         __uint_as_float(ra[2 * e + 1]) * p.scale_log2);
+                    own[16 + e] = pack2<true>(__uint_as_float(rb[2 * e]) * p.scale_log2,
+                                              __uint_as_float(rb[2 * e + 1]) * p.scale_log2);
                 }
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    st_shared_v4(sXout + x_off(row, c), own[4 * c], own[4 * c + 1], own[4 * c + 2],
+                                 own[4 * c + 3]);
                 fence_proxy_async();
             }
-            named_bar_sync(1, 128);
-            if (row == 0 && ok) {
-                // arm own receive barrier, then send the 32 KiB partial in one bulk copy
-                mbar_expect_tx(bar(C::B_XFULL), X_BYTES);
-                asm volatile(
-                    "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes"
-                    " [%0], [%1], %2, [%3];" ::"r"(peer_xin),
-                    "r"(sXout), "r"((uint32_t)X_BYTES), "r"(peer_xfull)
-                    : "memory");
-            }
+            named_bar_arrive(3, 160);  // staged: the courier warp sends it
+        };
+        if (ntiles > 0) stage(0);
+        // Every softmax thread runs every iteration and reaches every named
+        // barrier (those are not bounded in time); after a failed wait the
+        // remaining work is skipped.
+        for (int i = 0; i < ntiles; ++i) {
+            const int kp_next = (row < BN && i + 1 < ntiles) ? key_pos((i + 1) * BN + row) : INT_MAX;
             float s[64];
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar(C::B_XFULL), i & 1));
             if (ok) {
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
+                for (int c = 0; c < 8; ++c) {
                     const uint4 v = ld_shared_v4(sXin + x_off(row, c));
-                    const uint32_t *own = c < 8 ? &ra[4 * c] : &rb[4 * (c - 8)];
-                    s[4 * c] = __uint_as_float(own[0]) + __uint_as_float(v.x);
-                    s[4 * c + 1] = __uint_as_float(own[1]) + __uint_as_float(v.y);
-                    s[4 * c + 2] = __uint_as_float(own[2]) + __uint_as_float(v.z);
-                    s[4 * c + 3] = __uint_as_float(own[3]) + __uint_as_float(v.w);
+                    const uint32_t pw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&own[4 * c + e]));
+                        const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&pw[e]));
+                        s[8 * c + 2 * e] = a.x + b.x;
+                        s[8 * c + 2 * e + 1] = a.y + b.y;
+                    }
                 }
             }
-            named_bar_sync(1, 128);
-            if (row == 0 && ok) mbar_arrive_remote(peer_xtaken);  // X_in may be refilled
+            named_bar_arrive(2, 160);  // X_in read: the courier tells the peer
             if (ok) {
-                float tmax = -INFINITY;
-                const int32_t *kp = kpos + (i & 1) * BN;
+                const uint32_t kpa = hs::smem_addr(kpos + (i & 1) * BN);
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    const float v = kp[j] <= pos ? s[j] * p.scale_log2 : -INFINITY;
-                    s[j] = v;
-                    tmax = fmaxf(tmax, v);
+                for (int q = 0; q < 16; ++q) {
+                    const uint4 kv = ld_shared_v4(kpa + 16 * q);
+                    s[4 * q] = (int)kv.x <= pos ? s[4 * q] : -INFINITY;
+                    s[4 * q + 1] = (int)kv.y <= pos ? s[4 * q + 1] : -INFINITY;
+                    s[4 * q + 2] = (int)kv.z <= pos ? s[4 * q + 2] : -INFINITY;
+                    s[4 * q + 3] = (int)kv.w <= pos ? s[4 * q + 3] : -INFINITY;
                 }
+                // P and O are free once PV of the previous tile has finished
+                if (i > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_PVDONE), (i - 1) & 1));
+            }
+            if (ok) {
+                tc_fence_after();
+                float tmax = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < 64; ++j) tmax = fmaxf(tmax, s[j]);
                 if (i == 0) {
                     m2 = tmax;
                 } else {
@@ -484,19 +538,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     pk[e] = pack2<FP8>(a, c);
                 }
                 l += lsum;
-                // P overwrites the staged partial once the peer has taken it
-                ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar(C::B_XTAKEN), i & 1));
-                if (ok) {
-                    const uint32_t prow = sP + row * 128;
+                const uint32_t prow = sP + row * 128;
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        st_shared_v4(prow + ((q ^ (row & 7)) << 4), pk[4 * q], pk[4 * q + 1],
-                                     pk[4 * q + 2], pk[4 * q + 3]);
-                    fence_proxy_async();
-                    tc_fence_before();
-                    mbar_arrive(bar(C::B_PFULL));
-                }
+                for (int q = 0; q < 8; ++q)
+                    st_shared_v4(prow + ((q ^ (row & 7)) << 4), pk[4 * q], pk[4 * q + 1],
+                                 pk[4 * q + 2], pk[4 * q + 3]);
+                fence_proxy_async();
+                tc_fence_before();
+                mbar_arrive(bar(C::B_PFULL));
             }
+            // the next tile's exchange overlaps this tile's PV
+            if (i + 1 < ntiles) stage(i + 1);
             if (row < BN && i + 1 < ntiles) kpos[((i + 1) & 1) * BN + row] = kp_next;
         }
         if (ok && ntiles > 0) {
