@@ -59,3 +59,63 @@ class GpuWorkload:
         self.pool.sparse_mla_decode(q, self.gathered, self.gscale, self.resolved, t,
                                     self.req_ids, self.w.sm_scale, self.out, self.lse,
                                     self.workspace, stream)
+
+
+class GpuAgent:
+    """The agent mix in a GPU pool: all pages have a GPU block and a host copy;
+    each step maps only the pages its residency state keeps resident."""
+
+    def __init__(self, w: "W.AgentMix", stream=None):
+        self.w = w
+        lay = self.lay = W.agent_layout(w)
+        self.pool = hs.Pool(dtype=hs.HS_FP8_E4M3_ROWSCALE if w.dtype == "fp8" else hs.HS_BF16,
+                            n_gpu_blocks=lay.n_gpu_blocks, n_host_blocks=lay.n_host_blocks,
+                            max_requests=w.B, max_ctx=w.ctx, max_topk=w.K, hot_rows=w.hot_rows,
+                            stream=stream)
+        for r in range(w.B):
+            self.pool.request_init(r, w.first)
+            self.pool.hot_lease(r, lay.hot_blocks[r])
+        rows, scales = self.pool.gpu_rows(), self.pool.gpu_scales()
+        W.fill_rows(w.dtype, rows, scales, W.row_seed(w, "gpu"))  # hot blocks: arbitrary start
+        hr = torch.from_numpy(self.pool.host_rows())
+        hsc = self.pool.host_scales()
+        hst = None if hsc is None else torch.from_numpy(hsc)
+        W.fill_rows(w.dtype, hr, hst, W.row_seed(w, "host"), gen_device="cuda")
+        n = lay.n_host_blocks * 64  # GPU page blocks hold the same rows as their host copies
+        rows[:n].copy_(hr[:n])
+        if scales is not None:
+            scales[:n].copy_(hst[:n])
+        torch.cuda.synchronize()
+        self.page_gpu = np.full((w.B, w.pages), -1, np.int32)
+        dev = "cuda"
+        B, K, rb = w.B, w.K, w.row_bytes
+        self.req_ids = torch.arange(B, dtype=torch.int32, device=dev)
+        self.ctx = torch.empty(B, dtype=torch.int32, device=dev)
+        self.resolved = torch.empty((B, K), dtype=torch.int32, device=dev)
+        self.gathered = torch.empty((B, K, rb), dtype=torch.uint8, device=dev)
+        self.gscale = torch.empty((B, K), dtype=torch.float32, device=dev) if w.dtype == "fp8" else None
+        self.counts = torch.empty((B, 3), dtype=torch.int32, device=dev)
+        self.out = torch.empty((B, w.T, w.H, 512), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((B, w.T, w.H), dtype=torch.float32, device=dev)
+        ws = hs.hs_decode_workspace_bytes(B, w.T, w.H, K)
+        self.workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
+
+    def apply(self, st: "W.AgentStep"):
+        """Context lengths and the pages whose residency changed (host bookkeeping)."""
+        self.ctx.copy_(torch.from_numpy(st.ctx))
+        self.pool.set_ctx_lens(self.ctx)
+        for r in range(self.w.B):
+            diff = np.nonzero(st.page_gpu[r] != self.page_gpu[r])[0]
+            if diff.size:
+                a, b = int(diff[0]), int(diff[-1]) + 1
+                self.pool.page_map_range(r, a, st.page_gpu[r, a:b], self.lay.page_host[r, a:b])
+        self.page_gpu = st.page_gpu.copy()
+
+    def resolve(self, topk, stream=None):
+        self.pool.resolve_topk(self.req_ids, topk, self.resolved, self.gathered, self.gscale,
+                               self.counts, stream)
+
+    def decode(self, q, topk, stream=None):
+        self.pool.sparse_mla_decode(q, self.gathered, self.gscale, self.resolved, topk,
+                                    self.req_ids, self.w.sm_scale, self.out, self.lse,
+                                    self.workspace, stream)

@@ -229,6 +229,11 @@ class Pool:
     def set_ctx_len(self, req: int, ctx_len: int):
         _check("hs_request_set_ctx_len", load().hs_request_set_ctx_len(self.handle, req, ctx_len))
 
+    def set_ctx_lens(self, d_ctx_len, stream=None):
+        """Context lengths of requests 0..n-1 from an int32 CUDA tensor."""
+        _check("hs_set_ctx_len", load().hs_set_ctx_len(self.handle, _ptr(d_ctx_len),
+                                                       d_ctx_len.numel(), _stream(stream)))
+
     def page_map(self, req: int, page: int, gpu_block: int, host_block: int):
         _check("hs_page_map", load().hs_page_map(self.handle, req, page, gpu_block, host_block))
 

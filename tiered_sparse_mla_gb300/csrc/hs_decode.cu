@@ -239,16 +239,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             for (int c = 0; c < nq; ++c)
                 tma_load_3d(sQ + c * QCH_BYTES, &tm_q, 64 * (5 * half + c), mt * BM, b,
                             bar(C::B_QFULL));
-            if (half == 0) {  // stream this split's rows into L2 ahead of the tile loads
-                for (int i = 0; i < ntiles; ++i) {
-                    const int j = k0 + i * BN, n = min(BN, k1 - j);
-                    prefetch_l2(p.gathered + ((size_t)b * p.K + j) * p.row_bytes,
-                                (uint32_t)(n * p.row_bytes));
-                }
-            }
             int issued = 0;
             bool ok = true;
             for (int i = 0; i < ntiles && ok; ++i) {
+                if (i == NG && half == 0) {
+                    // the first groups are in flight: stream the rest of this
+                    // split's rows into L2 ahead of their tile loads
+                    for (int t = NG; t < ntiles; ++t) {
+                        const int j = k0 + t * BN, n = min(BN, k1 - j);
+                        prefetch_l2(p.gathered + ((size_t)b * p.K + j) * p.row_bytes,
+                                    (uint32_t)(n * p.row_bytes));
+                    }
+                }
                 const int g = i % NG;
                 const uint32_t ph = (uint32_t)(i / NG) & 1u;
                 if (!mbar_wait(bar(C::B_GEMPTY + g), ph ^ 1u) || misc[1]) {
@@ -287,14 +289,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     }
                     tc_fence_after();
                     const uint32_t dS = tmem + TM_S + (uint32_t)(i & 1) * BN;
+                    // descriptors advance by (bytes >> 4) in their low bits
+                    const uint64_t a0 = desc_sw128(sQ, 16, 1024);
+                    const uint64_t b0 = desc_sw128(slot(g, lc0), 16, 1024);
                     for (int lc = lc0; lc < NLC; ++lc) {
+                        const uint64_t ac = a0 + (uint64_t)(((lc - lc0) * QCH_BYTES) >> 4);
+                        const uint64_t bc = b0 + (uint64_t)(((lc - lc0) * KCH_BYTES) >> 4);
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint64_t a =
-                                desc_sw128(sQ + (lc - lc0) * QCH_BYTES + k * 32, 16, 1024);
-                            const uint64_t bd = desc_sw128(slot(g, lc) + k * 32, 16, 1024);
-                            mma_f16(dS, a, bd, ID_QK, (lc > lc0) || (k > 0));
-                        }
+                        for (int k = 0; k < 4; ++k)
+                            mma_f16(dS, ac + 2 * k, bc + 2 * k, ID_QK, (lc > lc0) || (k > 0));
                     }
                     mma_commit(bar(C::B_SFULL + (i & 1)));
                 }
@@ -305,12 +308,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         break;
                     }
                     tc_fence_after();
+                    const uint64_t pa = desc_sw128(sP, 16, 1024);
+                    const uint64_t vb = desc_sw128(slot(g, 0), KCH_BYTES, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {  // O[128 x 256] += P[:, 16kk..] V[16kk.., 0..256)
-                        const uint64_t a = desc_sw128(sP + kk * 32, 16, 1024);
-                        const uint64_t bd = desc_sw128(slot(g, 0) + kk * 2048, KCH_BYTES, 1024);
-                        mma_f16(tmem + TM_O, a, bd, ID_PV, (j > 0) || (kk > 0));
-                    }
+                    for (int kk = 0; kk < 4; ++kk)  // O[128 x 256] += P[:, 16kk..] V[16kk.., 0..256)
+                        mma_f16(tmem + TM_O, pa + 2 * kk, vb + 128 * kk, ID_PV, (j > 0) || (kk > 0));
                     mma_commit(bar(C::B_GEMPTY + g));
                     mma_commit(bar(C::B_PVDONE));
                 }

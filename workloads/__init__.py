@@ -299,3 +299,163 @@ def make_q(w: Workload, step: int, device="cpu"):
 
 def row_seed(w: Workload, tier: str) -> int:
     return w.seed * 1000003 + (1 if tier == "gpu" else 2)
+
+
+# ------------------------------------------------------------------ agent mix
+@dataclass(frozen=True)
+class AgentMix:
+    """Multi-turn agent-shaped mix, shaped like the benchmark of [A] 性能基准测试
+    (13 turns, 74,160-token first turn, +753 prefill tokens per later turn, 220
+    output tokens per turn, MTP3, FP8 KV). The traces themselves are not
+    available; only this shape is used.
+
+    Residency follows a seeded pressure schedule: u_r ~ U(0,1) once per request,
+    pi_t = (t-1)/(turns-1); in turn t a request is full-resident if u_r >= pi_t,
+    hybrid (resident tail of `resident_tail` tokens) if u_r >= pi_t/2, else none
+    (only the pages being written are resident). States only move full ->
+    hybrid -> none. Every page has a host copy (finished pages are copied to
+    host while still served from the GPU, [A] 关键架构细节, 主动复制), so a page
+    that stops being resident is still readable from host memory.
+
+    Decode step s of a turn that starts with `start` tokens sees context
+    L = start + T*(s+1): the T query tokens (1 + 3 MTP drafts, all accepted)
+    sit at positions L-T .. L-1."""
+
+    name: str = "agent"
+    index: int = 4
+    B: int = 32
+    turns: int = 13
+    first: int = 74160
+    per_turn: int = 753
+    out_tokens: int = 220
+    H: int = 128
+    T: int = 4
+    K: int = 2048
+    hot_rows: int = 4096
+    dtype: str = "fp8"
+    resident_tail: int = 32768
+    tail: int = 128          # last tokens always selected
+    reuse: float = 0.7
+    zipf_s: float = 1.0
+
+    @property
+    def seed(self) -> int:
+        return SEED_BASE + self.index
+
+    @property
+    def steps_per_turn(self) -> int:
+        return self.out_tokens // self.T
+
+    @property
+    def steps(self) -> int:
+        return self.turns * self.steps_per_turn
+
+    @property
+    def ctx(self) -> int:  # largest context any step sees
+        return self.turn_start(self.turns) + self.T * self.steps_per_turn
+
+    @property
+    def pages(self) -> int:
+        return (self.ctx + PAGE - 1) // PAGE
+
+    @property
+    def row_bytes(self) -> int:
+        return DIM * (2 if self.dtype == "bf16" else 1)
+
+    @property
+    def sm_scale(self) -> float:
+        return 1.0 / math.sqrt(DIM)
+
+    def turn_start(self, t: int) -> int:
+        return self.first + (t - 1) * (self.per_turn + self.out_tokens)
+
+    def scaled(self, **kw) -> "AgentMix":
+        return dataclasses.replace(self, **kw)
+
+
+@dataclass
+class AgentStep:
+    turn: int
+    step: int
+    ctx: np.ndarray        # int32 [B], context length at this step
+    state: np.ndarray      # int8 [B]: 0 full, 1 hybrid, 2 none
+    page_gpu: np.ndarray   # int32 [B][pages], -1 = not resident
+    topk: np.ndarray       # int32 [B][K]
+
+
+def agent_layout(w: AgentMix) -> Layout:
+    """Every page of request r has GPU block r*pages + page and host block
+    r*pages + page (the host copy); hot-buffer blocks follow all page blocks."""
+    P = w.pages
+    ids = (np.arange(w.B, dtype=np.int32)[:, None] * P + np.arange(P, dtype=np.int32)[None, :])
+    hb = w.hot_rows // PAGE
+    base = w.B * P
+    hot = (base + np.arange(w.B * hb, dtype=np.int32)).reshape(w.B, hb)
+    return Layout(ids.copy(), ids.copy(), hot, n_gpu_blocks=base + w.B * hb, n_host_blocks=w.B * P)
+
+
+def agent_steps(w: AgentMix) -> Iterator[AgentStep]:
+    """The agent mix, one decode step at a time (residency, context, top-K)."""
+    rng = np.random.Generator(np.random.PCG64(w.seed))
+    u = rng.random(w.B)
+    lay = agent_layout(w)
+    P = w.pages
+    full_cand = w.ctx - w.tail
+    zipf = _Zipf(full_cand, w.zipf_s)
+    perms = [rng.permutation(full_cand).astype(np.int32) for _ in range(w.B)]
+    taken = np.zeros(w.ctx, dtype=bool)
+    state = np.zeros(w.B, np.int8)
+    prev = [None] * w.B
+    n_body = w.K - w.tail
+    n_reuse = int(round(w.reuse * n_body))
+    page_idx = np.arange(P)
+    for t in range(1, w.turns + 1):
+        pi = (t - 1) / max(1, w.turns - 1)
+        new_state = np.where(u >= pi, 0, np.where(u >= pi / 2, 1, 2)).astype(np.int8)
+        state = np.maximum(state, new_state)  # full -> hybrid -> none only
+        start = w.turn_start(t)
+        for s in range(w.steps_per_turn):
+            L = start + w.T * (s + 1)
+            ctx = np.full(w.B, L, np.int32)
+            first_res = np.where(state == 0, 0,
+                                 np.where(state == 1, max(0, L - w.resident_tail) // PAGE,
+                                          (L - w.T) // PAGE))
+            page_gpu = np.where(page_idx[None, :] >= first_res[:, None], lay.page_gpu, -1)
+            page_gpu = page_gpu.astype(np.int32)
+            topk = np.empty((w.B, w.K), np.int32)
+            limit = L - w.tail  # body positions lie in [0, L - tail)
+            for r in range(w.B):
+                tail = np.arange(limit, L, dtype=np.int32)
+                keep = np.empty(0, np.int32)
+                if prev[r] is not None:
+                    cand = prev[r][prev[r] < limit]
+                    k = min(n_reuse, len(cand))
+                    keep = rng.choice(cand, size=k, replace=False).astype(np.int32)
+                taken[keep] = True
+                fresh = _zipf_below(zipf, rng, perms[r], n_body - len(keep), taken, limit)
+                body = np.concatenate([keep, fresh])
+                taken[body] = False
+                prev[r] = body
+                lst = np.concatenate([tail, body])
+                topk[r] = lst[rng.permutation(w.K)]
+            yield AgentStep(t, s, ctx, state.copy(), page_gpu, topk)
+
+
+def _zipf_below(zipf: _Zipf, rng, perm, k, taken, limit) -> np.ndarray:
+    """k distinct Zipf draws among positions < limit not marked in `taken`."""
+    out = []
+    need = k
+    while need > 0:
+        u = rng.random(max(4 * need, 64))
+        ranks = np.minimum(np.searchsorted(zipf.cdf, u, side="right"), zipf.n - 1)
+        pos = perm[ranks]
+        pos = pos[pos < limit]
+        _, first = np.unique(pos, return_index=True)
+        pos = pos[np.sort(first)]
+        pos = pos[~taken[pos]][:need]
+        taken[pos] = True
+        out.append(pos)
+        need -= len(pos)
+    res = np.concatenate(out).astype(np.int32) if out else np.empty(0, np.int32)
+    taken[res] = False
+    return res
