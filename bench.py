@@ -131,6 +131,38 @@ def algorithmic(w, counts_sum):
 
 
 # ------------------------------------------------------------------ GPU arm
+DESCS = {
+    "resident": WORKLOAD_DESC,
+    "tiny": ("tiny: 1 request x 4096-token context, pages 0-31 host-only and 32-63 resident, "
+             "BF16, 16 heads, 1 query token, top-K 256, hot buffer 512 rows"),
+    "hybrid": ("hybrid residency: 16 requests x 1,048,576-token context, last 32K tokens resident, "
+               "older pages in pinned host memory, FP8 e4m3 rows + fp32 scale, hot buffer 4096 "
+               "rows/request, 128 heads, MTP3 (4 query tokens), top-K 2048, 70% reuse per step"),
+    "noresident": ("no-resident prefix reuse: 32 requests x 524,288-token context all host-only, "
+                   "empty hot buffer at start, FP8 rows, 128 heads, top-K 2048 uniform, 50% reuse"),
+    "agent": ("multi-turn agent-shaped mix: 32 requests x 13 turns (74,160-token first turn, +753 "
+              "per turn, 220 output tokens), MTP3, FP8 rows, 128 heads, top-K 2048, residency "
+              "full/hybrid/none from a seeded pressure schedule"),
+}
+DEFAULT_STEPS = {"resident": 2000, "tiny": 2000, "hybrid": 512, "noresident": 256, "agent": 715}
+
+
+def _link_peak_gbs():
+    """Measured pinned host -> device copy bandwidth (best of 3, 256 MiB)."""
+    import torch
+    h = torch.empty(256 << 20, dtype=torch.uint8).pin_memory()
+    d = torch.empty_like(h, device="cuda")
+    best = 0.0
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        d.copy_(h, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        best = max(best, h.numel() / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    return best
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -144,18 +176,33 @@ def run_gpu(args):
     g.build()
     import tiered_sparse_mla_gb300 as hs
     import workloads as W
-    from harness import GpuWorkload
+    from harness import GpuAgent, GpuWorkload
 
-    w = W.WORKLOADS[WORKLOAD]
-    if args.batch != w.B:
+    name = args.workload
+    agent = name == "agent"
+    w = W.AgentMix() if agent else W.WORKLOADS[name]
+    if args.batch and args.batch != w.B:
         w = w.scaled(B=args.batch)
+    steps = args.steps or DEFAULT_STEPS[name]
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
-        gw = GpuWorkload(w, stream=stream)
-        qs = [W.make_q(w, s, device="cuda") for s in range(w.steps)]
+        if agent:
+            gw = GpuAgent(w, stream=stream)
+            plan = list(W.agent_steps(w))
+            lists = [torch.from_numpy(st.topk).to("cuda") for st in plan]
+        else:
+            gw = GpuWorkload(w, stream=stream)
+            plan = None
+            lists = [gw.topk[s] for s in range(w.steps)]
+        nq = min(len(lists), 16)
+        qs = [W.make_q(w, s, device="cuda") for s in range(nq)]
         flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
         flush_rd = torch.ones(64 << 20, dtype=torch.float32, device="cuda")
     torch.cuda.synchronize()
+    if agent:
+        gw.apply(plan[0])
+    snap = gw.pool.snapshot()
+    n_lists = len(lists)
 
     def l2_flush():
         # write 256 MiB (evicts everything), then read 256 MiB of other data so
@@ -163,27 +210,42 @@ def run_gpu(args):
         flush.zero_()
         flush_rd.sum()
 
+    def prepare(s):
+        """Untimed bookkeeping before step s: residency/context updates of the
+        agent mix, and the hot-buffer state restored when the step list wraps."""
+        i = s % n_lists
+        if i == 0 and s > 0:
+            torch.cuda.synchronize()
+            gw.pool.restore(snap)
+        if agent:
+            gw.apply(plan[i])
+
     def step(s, ev=None):
-        t = gw.topk[s % w.steps]
+        t = lists[s % n_lists]
+        q = qs[s % nq]
         if ev is not None:
             ev[0].record(stream)
         gw.pool.resolve_topk(gw.req_ids, t, gw.resolved, gw.gathered, gw.gscale, gw.counts, stream)
         if ev is not None:
             ev[1].record(stream)
-        gw.pool.sparse_mla_decode(qs[s % w.steps], gw.gathered, gw.gscale, gw.resolved, t,
-                                  gw.req_ids, w.sm_scale, gw.out, gw.lse, gw.workspace, stream)
+        gw.pool.sparse_mla_decode(q, gw.gathered, gw.gscale, gw.resolved, t, gw.req_ids,
+                                  w.sm_scale, gw.out, gw.lse, gw.workspace, stream)
         if ev is not None:
             ev[2].record(stream)
 
     with torch.cuda.stream(stream):
         for s in range(args.warmup):
+            prepare(s)
             l2_flush()
             step(s)
     torch.cuda.synchronize()
     assert gw.pool.get_error() == 0
+    # timed steps start from the beginning of the step list and its initial state
+    gw.pool.restore(snap)
+    if agent:
+        gw.apply(plan[0])
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    cnt_sum = np.zeros(3, np.int64)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     counts_acc = torch.zeros(3, dtype=torch.int64, device="cuda")
     if ws > 1:
         import torch.distributed as dist
@@ -192,9 +254,11 @@ def run_gpu(args):
     t0 = time.perf_counter()
     with ClockSampler(local) as clk, torch.cuda.stream(stream):
         torch.cuda.nvtx.range_push("timed_region")
-        for s in range(args.steps):
+        for s in range(steps):
+            if s > 0:
+                prepare(s)
             l2_flush()
-            step(args.warmup + s, evs[s])
+            step(s, evs[s])
             counts_acc += gw.counts.sum(0)
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
@@ -203,19 +267,19 @@ def run_gpu(args):
         dist.barrier()
     assert gw.pool.get_error() == 0
     cnt_sum = counts_acc.cpu().numpy()
-    t_res = [evs[s][0].elapsed_time(evs[s][1]) for s in range(args.steps)]
-    t_dec = [evs[s][1].elapsed_time(evs[s][2]) for s in range(args.steps)]
-    ms_step = (sum(t_res) + sum(t_dec)) / args.steps
+    t_res = [evs[s][0].elapsed_time(evs[s][1]) for s in range(steps)]
+    t_dec = [evs[s][1].elapsed_time(evs[s][2]) for s in range(steps)]
+    ms_step = (sum(t_res) + sum(t_dec)) / steps
     if ws > 1:
         tt = torch.tensor([ms_step], device="cuda")
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms_step = float(tt.item())
     steps_per_s = ws / (ms_step * 1e-3)
-    res_ms = sum(t_res) / args.steps
-    dec_ms = sum(t_dec) / args.steps
+    res_ms = sum(t_res) / steps
+    dec_ms = sum(t_dec) / steps
     rows_per_s = ws * w.B * w.K / (res_ms * 1e-3)
 
-    per_step_counts = cnt_sum / args.steps
+    per_step_counts = cnt_sum / steps
     r_hbm, r_link, d_bytes, flops = algorithmic(w, per_step_counts)
     hbm_peak, tf_peak, peak_kind = _peaks()
     kernels = {
@@ -227,6 +291,8 @@ def run_gpu(args):
                    "tflops": flops / (dec_ms * 1e-3) / 1e12,
                    "traffic": _traffic("decode", "tiered_sparse_mla_gb300/csrc/hs_decode.cu")},
     }
+    if name != WORKLOAD or w.B != W.WORKLOADS[WORKLOAD].B:
+        kernels["resolve"]["traffic"] = kernels["decode"]["traffic"] = None  # captured on another workload
     # the decode's roofline time is max(bytes / BW, flops / tensor peak)
     t_bytes = d_bytes / (hbm_peak * 1e9)
     t_flops = flops / (tf_peak * 1e12)
@@ -240,16 +306,15 @@ def run_gpu(args):
                 "frac": round(kt["achieved"] / kt["peak"], 4), "traffic": kt["traffic"],
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"}
 
-    # ---- end to end through the C ABI with host buffers (pinned), per step
-    e2e = run_e2e(args, gw, qs, stream, w)
     launches = 2 + (1 if hs.hs_decode_workspace_bytes(w.B, w.T, w.H, w.K) > 0 else 0)
+    desc = DESCS[name] if (agent or w.B == W.WORKLOADS[name].B) else f"{DESCS[name]} [batch {w.B}]"
     line = {
         "metric": METRIC, "value": round(steps_per_s, 2), "unit": "decode steps/s",
-        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "n_gpus": ws, "steps": steps, "warmup": args.warmup,
         "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC if w.B == 32 else f"{WORKLOAD_DESC} [batch {w.B}]",
-                   "global_batch": w.B * ws, "top_k": w.K,
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "fp8 rows, f16 MMA",
+        "data": "synthetic",
+        "config": {"workload": desc, "global_batch": w.B * ws, "top_k": w.K,
                    "heads": w.H, "query_tokens": w.T, "ctx": w.ctx,
                    "parallelism": f"replicas x{ws} (requests sharded by rank, no collective)",
                    "l2": ("flushed before every timed step: 256 MiB written, then 256 MiB of "
@@ -261,10 +326,26 @@ def run_gpu(args):
         "roofline": roofline,
         "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
                     for k, v in kernels.items()},
-        "e2e": e2e, "gpu_launches": launches * args.steps,
+        "gpu_launches": launches * steps,
         "clocks": clk.summary(), "wall_s": round(wall, 3),
     }
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+    if r_link > 0:
+        link_peak = _link_peak_gbs()
+        ach = r_link / (res_ms * 1e-3) / 1e9
+        line["host_link"] = {"miss_bytes_per_step": r_link, "achieved": round(ach, 1),
+                             "peak": round(link_peak, 1), "unit": "GB/s",
+                             "frac": round(ach / link_peak, 4),
+                             "peak_source": "measured live: pinned 256 MiB host-to-device copy"}
+    if agent:
+        per_turn = []
+        for t in range(w.turns):
+            a, b = t * w.steps_per_turn, min(steps, (t + 1) * w.steps_per_turn)
+            if a < b:
+                per_turn.append(round(sum(t_res[a:b]) + sum(t_dec[a:b]), 3))
+        line["per_turn_ms"] = per_turn
+    if name == WORKLOAD and not agent:
+        line["e2e"] = run_e2e(args, gw, qs, stream, w)
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and name == WORKLOAD:
         line["cpu_baseline"] = cpu_baseline(w, args)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -279,7 +360,7 @@ def run_e2e(args, gw, qs, stream, w):
     import torch
     n = min(args.steps, 200)
     topk_h = [gw.topk[s % w.steps].cpu().pin_memory() for s in range(w.steps)]
-    q_h = [qs[s % w.steps].cpu().pin_memory() for s in range(w.steps)]
+    q_h = [q.cpu().pin_memory() for q in qs]
     out_h = torch.empty(gw.out.shape, dtype=gw.out.dtype).pin_memory()
     lse_h = torch.empty(gw.lse.shape, dtype=gw.lse.dtype).pin_memory()
     t_d = torch.empty_like(gw.topk[0])
@@ -289,7 +370,7 @@ def run_e2e(args, gw, qs, stream, w):
     with torch.cuda.stream(stream):
         for s in range(3):
             t_d.copy_(topk_h[s], non_blocking=True)
-            q_d.copy_(q_h[s], non_blocking=True)
+            q_d.copy_(q_h[s % len(q_h)], non_blocking=True)
             gw.pool.resolve_topk(gw.req_ids, t_d, gw.resolved, gw.gathered, gw.gscale, gw.counts, stream)
             gw.pool.sparse_mla_decode(q_d, gw.gathered, gw.gscale, gw.resolved, t_d, gw.req_ids,
                                       w.sm_scale, gw.out, gw.lse, gw.workspace, stream)
@@ -300,7 +381,7 @@ def run_e2e(args, gw, qs, stream, w):
         e0.record(stream)
         for s in range(n):
             t_d.copy_(topk_h[s % w.steps], non_blocking=True)
-            q_d.copy_(q_h[s % w.steps], non_blocking=True)
+            q_d.copy_(q_h[s % len(q_h)], non_blocking=True)
             gw.pool.resolve_topk(gw.req_ids, t_d, gw.resolved, gw.gathered, gw.gscale, gw.counts, stream)
             gw.pool.sparse_mla_decode(q_d, gw.gathered, gw.gscale, gw.resolved, t_d, gw.req_ids,
                                       w.sm_scale, gw.out, gw.lse, gw.workspace, stream)
@@ -421,17 +502,21 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=0,
+                    help="timed steps (default: 2000 for the resident workload)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work spent on the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--batch", type=int, default=32,
-                    help="requests per step (32 = the workload; smaller only for profiling)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="requests per step (default: the workload's; smaller only for profiling)")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(DESCS),
+                    help="resident (default, the headline) or another configuration")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    args.steps = args.steps or DEFAULT_STEPS[args.workload]
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -15,20 +15,25 @@
 // checked before the hot buffer; a missing position repeated in one list is
 // served once (first in list order).
 //
-// Design (GB300): one thread-block cluster of G CTAs per request.
-//   phase 1  every CTA classifies its K/G entries (page table, then
-//            pos_to_slot), stamps its hot hits and lists its misses in shared
-//            memory;                                    -> cluster barrier A
-//   rank 0   merges all CTAs' miss lists over distributed shared memory, sorts
-//            them (bitonic, in shared memory), picks victims from the
-//            persistent per-request LRU order (slots kept sorted by
-//            (stamp, slot), so the i-th unprotected entry is the i-th victim),
-//            updates tag / stamp / pos_to_slot / LRU order and writes each
-//            miss's slot back into its owner CTA's shared memory;
-//   others   meanwhile copy their resident and hot rows (16-byte vectors,
-//            several loads in flight per thread);       -> cluster barrier B
-//   phase 3  every CTA copies its miss rows from the device-mapped pinned host
-//            arena into the slot and into the gathered buffer.
+// Design (GB300): one thread-block cluster of G CTAs per request. Rank 0 keeps
+// the request's LRU bookkeeping; ranks 1..G-1 ("workers") own K/(G-1) list
+// entries each.
+//   start    cluster barrier (every CTA's shared memory is live);
+//   phase 1  workers classify their entries (page table, then pos_to_slot),
+//            stamp their hot hits, and push each miss's (position, list index)
+//            key straight into rank 0's shared memory; -> cluster barrier A
+//   rank 0   sorts the keys (bitonic, in shared memory), ranks distinct
+//            positions, stages the persistent LRU order (slots kept sorted by
+//            (stamp, slot), so the i-th unprotected entry is the i-th victim)
+//            in shared memory, places the misses (tag / stamp / pos_to_slot /
+//            LRU order) and writes each miss's slot into its owner's shared
+//            memory;
+//   phase 2  meanwhile workers copy every row whose gathered position is known
+//            -- resident and hot rows from the pool, miss rows from the
+//            device-mapped pinned host arena -- into the gathered buffer, so
+//            the host-link reads overlap rank 0's bookkeeping; -> barrier B
+//   phase 3  workers copy each placed miss row from the gathered buffer into
+//            its hot slot (HBM to HBM) and zero rejected ones.
 // Barriers are hardware cluster barriers: no spin loops.
 #include <cstdint>
 
@@ -42,25 +47,33 @@ constexpr int KIND_NONE = 0, KIND_RES = 1, KIND_HOT = 2, KIND_MISS = 3;
 
 // Dynamic shared memory layout (bytes), identical in every CTA.
 struct Smem {
-    int chunk, kpad, K;
+    int chunk, kpad, K, C, W;  // W = workers = G - 1
+    // worker part
     __host__ __device__ size_t off_src() const { return 0; }
     __host__ __device__ size_t off_hrow() const { return off_src() + 4 * (size_t)chunk; }
     __host__ __device__ size_t off_kind() const { return off_hrow() + 4 * (size_t)chunk; }
     __host__ __device__ size_t off_mj() const { return off_kind() + 4 * (size_t)chunk; }
-    __host__ __device__ size_t off_mp() const { return off_mj() + 4 * (size_t)chunk; }
-    __host__ __device__ size_t off_misc() const { return off_mp() + 4 * (size_t)chunk; }
-    // misc: [0] local misses, [1] local resident, [2] local hot, [3..3+16) offsets,
-    //       [20..20+32) warp scan scratch
-    __host__ __device__ size_t off_keys() const { return (off_misc() + 4 * 64 + 15) & ~size_t(15); }
+    // misc: [0] local misses, [1..3] worker totals, [20..52) warp scan scratch,
+    //       [64 + 4g + 0..2] {misses, resident, hot} of worker g (rank 0 only)
+    __host__ __device__ size_t off_misc() const { return off_mj() + 4 * (size_t)chunk; }
+    // rank-0 part
+    __host__ __device__ size_t off_kin() const { return (off_misc() + 4 * 128 + 15) & ~size_t(15); }
+    __host__ __device__ size_t off_keys() const { return off_kin() + 8 * (size_t)W * chunk; }
     __host__ __device__ size_t off_rank() const { return off_keys() + 8 * (size_t)kpad; }
     __host__ __device__ size_t off_victim() const { return off_rank() + 4 * (size_t)K; }
-    __host__ __device__ size_t total() const { return off_victim() + 4 * (size_t)K; }
+    __host__ __device__ size_t off_lru() const { return off_victim() + 4 * (size_t)K; }
+    __host__ __device__ size_t off_prot() const { return off_lru() + 4 * (size_t)C; }
+    __host__ __device__ size_t total() const { return off_prot() + (size_t)C; }
 };
 
 __host__ __device__ inline int next_pow2(int x) {
     int p = 1;
     while (p < x) p <<= 1;
     return p;
+}
+
+__device__ __forceinline__ void dsmem_st64(uint32_t a, unsigned long long v) {
+    asm volatile("st.shared::cluster.u64 [%0], %1;\n" ::"r"(a), "l"(v) : "memory");
 }
 
 template <int RB>
@@ -71,25 +84,29 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
                float *__restrict__ gscale, int32_t *__restrict__ counts) {
     constexpr int V = RB / 16;  // 16-byte vectors per row
     extern __shared__ __align__(16) unsigned char smem[];
-    const Smem L{chunk, next_pow2(K), K};
+    const int W = G - 1;
+    const Smem L{chunk, next_pow2(K), K, P.C, W};
     int32_t *s_src = reinterpret_cast<int32_t *>(smem + L.off_src());
     int32_t *s_hrow = reinterpret_cast<int32_t *>(smem + L.off_hrow());
     int32_t *s_kind = reinterpret_cast<int32_t *>(smem + L.off_kind());
     int32_t *s_mj = reinterpret_cast<int32_t *>(smem + L.off_mj());
-    int32_t *s_mp = reinterpret_cast<int32_t *>(smem + L.off_mp());
     int32_t *s_misc = reinterpret_cast<int32_t *>(smem + L.off_misc());
     int32_t *s_warp = s_misc + 20;
+    int32_t *s_wcnt = s_misc + 64;  // [G][4], filled by the workers (rank 0 only)
+    unsigned long long *s_kin = reinterpret_cast<unsigned long long *>(smem + L.off_kin());
     unsigned long long *s_keys = reinterpret_cast<unsigned long long *>(smem + L.off_keys());
     int32_t *s_rank = reinterpret_cast<int32_t *>(smem + L.off_rank());
     int32_t *s_victim = reinterpret_cast<int32_t *>(smem + L.off_victim());
+    int32_t *s_lru = reinterpret_cast<int32_t *>(smem + L.off_lru());
+    uint8_t *s_prot = smem + L.off_prot();
 
     const int tid = threadIdx.x;
     const int g = static_cast<int>(hs::cluster_ctarank());
     const int bi = blockIdx.y;
     const int r = req_ids[bi];
-    const int j0 = g * chunk;
-    const int nloc = max(0, min(K, j0 + chunk) - j0);
-    const size_t row0 = (size_t)bi * K + j0;  // first gathered row of this CTA
+    const int j0 = (g - 1) * chunk;  // first list entry of a worker
+    const int nloc = g == 0 ? 0 : max(0, min(K, j0 + chunk) - j0);
+    const size_t row0 = (size_t)bi * K + (g == 0 ? 0 : j0);  // first gathered row of this CTA
     const bool fp8 = gscale != nullptr;
 
     if (r < 0 || r >= P.max_req) {
@@ -116,82 +133,169 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
     int32_t *p2s = P.p2s + (size_t)r * P.max_ctx;
 
     if (tid == 0) s_misc[0] = s_misc[1] = s_misc[2] = 0;
+    // every CTA of the cluster is running (and has set up its shared memory)
+    // before any distributed-shared-memory store below
     __syncthreads();
+    hs::cluster_arrive();
+    hs::cluster_wait();
 
-    // ---------------------------------------------------------------- phase 1
     uint32_t err = 0;
-    int n_res = 0, n_hot = 0;
-    for (int l = tid; l < nloc; l += NT) {
-        const int p = topk[row0 + l];
-        int kind = KIND_NONE, src = -1, hrow = -1;
-        if (p == -1) {
-        } else if (p < 0 || p >= Lr || p >= P.max_ctx) {
-            err |= HS_DEVERR_INDEX_RANGE;
-        } else {
-            const int2 e = page[p >> 6];
-            if (e.x >= 0) {
-                kind = KIND_RES;
-                src = e.x * hs::kPage + (p & 63);
-                ++n_res;
+    if (g != 0) {
+        // ------------------------------------------------------------ phase 1
+        const uint32_t kin0 = hs::dsmem_map(s_kin + (size_t)(g - 1) * chunk, 0);
+        int n_res = 0, n_hot = 0;
+        for (int l = tid; l < nloc; l += NT) {
+            const int p = topk[row0 + l];
+            int kind = KIND_NONE, src = -1, hrow = -1;
+            if (p == -1) {
+            } else if (p < 0 || p >= Lr || p >= P.max_ctx) {
+                err |= HS_DEVERR_INDEX_RANGE;
             } else {
-                const int s = p2s[p];
-                if (s >= 0) {
-                    kind = KIND_HOT;
-                    src = hblk[s >> 6] * hs::kPage + (s & 63);
-                    stamp[s] = c;
-                    ++n_hot;
-                } else if (e.y < 0) {
-                    err |= HS_DEVERR_NO_HOST;
+                const int2 e = page[p >> 6];
+                if (e.x >= 0) {
+                    kind = KIND_RES;
+                    src = e.x * hs::kPage + (p & 63);
+                    ++n_res;
                 } else {
-                    kind = KIND_MISS;
-                    hrow = e.y * hs::kPage + (p & 63);
-                    const int m = atomicAdd(&s_misc[0], 1);
-                    s_mj[m] = l;
-                    s_mp[m] = p;
+                    const int s = p2s[p];
+                    if (s >= 0) {
+                        kind = KIND_HOT;
+                        src = hblk[s >> 6] * hs::kPage + (s & 63);
+                        stamp[s] = c;
+                        ++n_hot;
+                    } else if (e.y < 0) {
+                        err |= HS_DEVERR_NO_HOST;
+                    } else {
+                        kind = KIND_MISS;
+                        hrow = e.y * hs::kPage + (p & 63);
+                        const int m = atomicAdd(&s_misc[0], 1);
+                        s_mj[m] = l;
+                        dsmem_st64(kin0 + 8u * (uint32_t)m,
+                                   ((unsigned long long)(uint32_t)p << 32) | (uint32_t)(j0 + l));
+                    }
+                }
+            }
+            s_kind[l] = kind;
+            s_src[l] = src;
+            s_hrow[l] = hrow;
+        }
+        if (n_res) atomicAdd(&s_misc[1], n_res);
+        if (n_hot) atomicAdd(&s_misc[2], n_hot);
+        __syncthreads();
+        // this worker's totals into rank 0 (one writer per slot)
+        if (tid < 3) hs::dsmem_st(hs::dsmem_map(&s_wcnt[4 * g + tid], 0), s_misc[tid]);
+        __threadfence();  // hot-hit stamps visible to rank 0 before barrier A
+        __syncthreads();
+        hs::cluster_arrive();  // barrier A
+
+        // ------------------------------------------------------------ phase 2
+        // every row whose gathered position is known: pool rows for hits, host
+        // rows for misses (placed into their slots after barrier B), zeros
+        {
+            const int nunits = nloc * V;
+            uint8_t *gdst = gathered + row0 * RB;
+            for (int base = tid; base < nunits; base += NT * UNROLL) {
+                uint4 v[UNROLL];
+#pragma unroll
+                for (int u = 0; u < UNROLL; ++u) {
+                    const int i = base + u * NT;
+                    v[u] = make_uint4(0, 0, 0, 0);
+                    if (i < nunits) {
+                        const int l = i / V, part = i - l * V;
+                        const int kd = s_kind[l];
+                        if (kd == KIND_RES || kd == KIND_HOT)
+                            v[u] = hs::ld_stream_v4(P.rows + (size_t)s_src[l] * RB + part * 16);
+                        else if (kd == KIND_MISS)
+                            v[u] = hs::ld_v4(P.host_rows + (size_t)s_hrow[l] * RB + part * 16);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < UNROLL; ++u)
+                    if (base + u * NT < nunits) hs::st_v4(gdst + (size_t)(base + u * NT) * 16, v[u]);
+            }
+            for (int l = tid; l < nloc; l += NT) {
+                const int kd = s_kind[l];
+                if (kd != KIND_MISS) resolved[row0 + l] = kd == KIND_NONE ? -1 : s_src[l];
+                if (fp8) {
+                    float sc = 0.f;
+                    if (kd == KIND_RES || kd == KIND_HOT) sc = P.scales[s_src[l]];
+                    else if (kd == KIND_MISS) sc = P.host_scales[s_hrow[l]];
+                    gscale[row0 + l] = sc;
                 }
             }
         }
-        s_kind[l] = kind;
-        s_src[l] = src;
-        s_hrow[l] = hrow;
-    }
-    if (n_res) atomicAdd(&s_misc[1], n_res);
-    if (n_hot) atomicAdd(&s_misc[2], n_hot);
-    __threadfence();  // hot-hit stamps visible to rank 0 before barrier A
-    __syncthreads();
-    hs::cluster_arrive();  // barrier A
+        hs::cluster_wait();    // barrier A (long complete)
+        hs::cluster_arrive();  // barrier B
+        hs::cluster_wait();    // barrier B: rank 0 has placed every miss
 
-    if (g == 0) {
+        // ------------------------------------------------------------ phase 3
+        // placed miss rows: gathered -> hot slot; rejected ones: zeroed
+        {
+            __syncthreads();  // this CTA's gathered writes are visible to all its threads
+            const int nm = s_misc[0];
+            const int nunits = nm * V;
+            uint8_t *gsrc = gathered + row0 * RB;
+            for (int base = tid; base < nunits; base += NT * UNROLL) {
+                uint4 v[UNROLL];
+                int dst[UNROLL], l_[UNROLL], part_[UNROLL];
+#pragma unroll
+                for (int u = 0; u < UNROLL; ++u) {
+                    const int i = base + u * NT;
+                    dst[u] = -2;
+                    if (i < nunits) {
+                        const int mi = i / V, part = i - mi * V;
+                        const int l = s_mj[mi];
+                        l_[u] = l;
+                        part_[u] = part;
+                        dst[u] = s_src[l];
+                        if (dst[u] >= 0) v[u] = hs::ld_v4(gsrc + (size_t)l * RB + part * 16);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < UNROLL; ++u) {
+                    if (dst[u] >= 0)
+                        hs::st_v4(P.rows + (size_t)dst[u] * RB + part_[u] * 16, v[u]);
+                    else if (dst[u] == -1)
+                        hs::st_v4(gsrc + (size_t)l_[u] * RB + part_[u] * 16, make_uint4(0, 0, 0, 0));
+                }
+            }
+            for (int mi = tid; mi < nm; mi += NT) {
+                const int l = s_mj[mi];
+                const int d = s_src[l];
+                resolved[row0 + l] = d;
+                if (fp8) {
+                    if (d >= 0) P.scales[d] = gscale[row0 + l];
+                    else gscale[row0 + l] = 0.f;
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ rank 0
+        hs::cluster_arrive();  // barrier A
         hs::cluster_wait();
-        // ------------------------------------------------ rank 0: LRU update
-        int32_t *s_off = s_misc + 3;
+        int32_t *s_off = s_misc + 4;  // [0..W] miss offsets of the workers, then totals
         if (tid == 0) {
             int acc = 0, res = 0, hot = 0;
-            for (int q = 0; q < G; ++q) {
-                s_off[q] = acc;
-                acc += hs::dsmem_ld(hs::dsmem_map(&s_misc[0], q));
-                res += hs::dsmem_ld(hs::dsmem_map(&s_misc[1], q));
-                hot += hs::dsmem_ld(hs::dsmem_map(&s_misc[2], q));
+            for (int q = 1; q <= W; ++q) {
+                s_off[q - 1] = acc;
+                acc += s_wcnt[4 * q];
+                res += s_wcnt[4 * q + 1];
+                hot += s_wcnt[4 * q + 2];
             }
-            s_off[G] = acc;
-            s_off[G + 1] = res;
-            s_off[G + 2] = hot;
+            s_off[W] = acc;
+            s_off[W + 1] = res;
+            s_off[W + 2] = hot;
         }
         __syncthreads();
-        const int n_miss = s_off[G], tot_res = s_off[G + 1], tot_hot = s_off[G + 2];
+        const int n_miss = s_off[W], tot_res = s_off[W + 1], tot_hot = s_off[W + 2];
         const bool leased = hblk[0] >= 0;
         int served = 0;
         if (n_miss > 0 || tot_hot > 0) {
-            // gather (position, list index) keys from every CTA's miss list
-            for (int q = 0; q < G; ++q) {
-                const int nq = s_off[q + 1] - s_off[q];
-                const uint32_t mj = hs::dsmem_map(s_mj, q), mp = hs::dsmem_map(s_mp, q);
-                for (int i = tid; i < nq; i += NT) {
-                    const int l = hs::dsmem_ld(mj + 4 * i);
-                    const int p = hs::dsmem_ld(mp + 4 * i);
-                    s_keys[s_off[q] + i] =
-                        ((unsigned long long)(uint32_t)p << 32) | (uint32_t)(q * chunk + l);
-                }
+            // dense key array from the workers' regions
+            for (int q = 1; q <= W; ++q) {
+                const int nq = s_off[q] - s_off[q - 1];
+                for (int i = tid; i < nq; i += NT)
+                    s_keys[s_off[q - 1] + i] = s_kin[(size_t)(q - 1) * chunk + i];
             }
             const int n2 = next_pow2(n_miss);
             for (int i = n_miss + tid; i < n2; i += NT) s_keys[i] = ~0ull;
@@ -199,7 +303,7 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
             for (int k = 2; k <= n2; k <<= 1) {  // bitonic sort, ascending
                 for (int jj = k >> 1; jj > 0; jj >>= 1) {
                     for (int i = tid; i < (n2 >> 1); i += NT) {
-                        const int lo = (i / jj) * 2 * jj + (i % jj), hi = lo + jj;
+                        const int lo = ((i & ~(jj - 1)) << 1) | (i & (jj - 1)), hi = lo + jj;
                         const unsigned long long a = s_keys[lo], b = s_keys[hi];
                         if ((a > b) == ((lo & k) == 0)) {
                             s_keys[lo] = b;
@@ -221,30 +325,58 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
                 if (i < n_miss) s_rank[i] = first ? m + pre : -1;
                 m += tot;
             }
+            // stage the LRU order with each slot's protection in shared memory
+            // (all loads in flight at once): bit 31 set = unprotected
+            for (int i0 = 0; i0 < C; i0 += NT * 8) {
+                int o[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int i = i0 + e * NT + tid;
+                    o[e] = i < C ? lru[i] : 0;
+                }
+                int st[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) st[e] = (i0 + e * NT + tid) < C ? stamp[o[e]] : 0;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int i = i0 + e * NT + tid;
+                    if (i < C) {
+                        const int u = st[e] < c;
+                        s_lru[i] = o[e] | (u ? int(0x80000000u) : 0);
+                        s_prot[o[e]] = u ? 0 : 1;
+                    }
+                }
+            }
+            __syncthreads();
             // walk the LRU order: the first m unprotected slots are the victims,
-            // the remaining unprotected slots move to the front (in place)
+            // the remaining unprotected slots move to the front
             int nu = 0;
             const int mv = leased ? m : 0;
             for (int base = 0; base < C; base += NT) {
                 const int i = base + tid;
                 int o = -1, u = 0;
                 if (i < C) {
-                    o = lru[i];
-                    u = stamp[o] < c;
+                    const int v = s_lru[i];
+                    o = v & 0x7fffffff;
+                    u = v < 0;
                 }
                 int tot;
                 const int pre = hs::block_scan_flag<NT>(u, s_warp, tot);
                 if (u) {
                     const int k = nu + pre;
-                    if (k < mv) s_victim[k] = o;
-                    else lru[k - mv] = o;
+                    if (k < mv) {
+                        s_victim[k] = o;
+                        s_prot[o] = 1;  // stamped this step once placed
+                    } else {
+                        lru[k - mv] = o;
+                    }
                 }
                 nu += tot;
             }
             const int mvict = min(mv, nu);
             served = mvict;
             __syncthreads();
-            // place the misses; tell each owner CTA its slot row (-1 = rejected)
+            // place the misses; tell each owner worker its slot row (-1 = rejected)
             for (int i = tid; i < n_miss; i += NT) {
                 const unsigned long long key = s_keys[i];
                 const int p = static_cast<int>(key >> 32), j = static_cast<int>(key & 0xffffffffu);
@@ -263,15 +395,15 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
                     p2s[p] = v;
                     dst = hblk[v >> 6] * hs::kPage + (v & 63);
                 }
-                const int owner = j / chunk;
-                hs::dsmem_st(hs::dsmem_map(&s_src[j - owner * chunk], owner), dst);
+                const int owner = 1 + j / chunk;
+                hs::dsmem_st(hs::dsmem_map(&s_src[j - (owner - 1) * chunk], owner), dst);
             }
             __syncthreads();
             // the slots stamped this step, in slot order, close the LRU order
             int out = nu - mvict;
             for (int base = 0; base < C; base += NT) {
                 const int s = base + tid;
-                const int f = (s < C) && stamp[s] == c;
+                const int f = (s < C) && s_prot[s];
                 int tot;
                 const int pre = hs::block_scan_flag<NT>(f, s_warp, tot);
                 if (f) lru[out + pre] = s;
@@ -287,107 +419,24 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
         __threadfence();
         __syncthreads();
         hs::cluster_arrive();  // barrier B: miss slots published
-    }
-
-    // ---------------------------------------------- phase 2: resident and hot rows
-    {
-        const int nunits = nloc * V;
-        uint8_t *gdst = gathered + row0 * RB;
-        for (int base = tid; base < nunits; base += NT * UNROLL) {
-            uint4 v[UNROLL];
-            int act[UNROLL];
-#pragma unroll
-            for (int u = 0; u < UNROLL; ++u) {
-                const int i = base + u * NT;
-                act[u] = 0;
-                if (i < nunits) {
-                    const int l = i / V, part = i - l * V;
-                    const int kd = s_kind[l];
-                    if (kd == KIND_RES || kd == KIND_HOT) {
-                        v[u] = hs::ld_stream_v4(P.rows + (size_t)s_src[l] * RB + part * 16);
-                        act[u] = 1;
-                    } else if (kd == KIND_NONE) {
-                        v[u] = make_uint4(0, 0, 0, 0);
-                        act[u] = 1;
-                    }
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < UNROLL; ++u)
-                if (act[u]) hs::st_v4(gdst + (size_t)(base + u * NT) * 16, v[u]);
-        }
-        for (int l = tid; l < nloc; l += NT) {
-            const int kd = s_kind[l];
-            if (kd == KIND_MISS) continue;
-            resolved[row0 + l] = kd == KIND_NONE ? -1 : s_src[l];
-            if (fp8) gscale[row0 + l] = kd == KIND_NONE ? 0.f : P.scales[s_src[l]];
-        }
-    }
-
-    if (g != 0) {
-        hs::cluster_wait();    // barrier A (long complete)
-        hs::cluster_arrive();  // barrier B
-    }
-    hs::cluster_wait();  // barrier B: rank 0 has placed every miss
-
-    // ---------------------------------------------- phase 3: miss rows from host
-    {
-        const int nm = s_misc[0];
-        uint8_t *gdst = gathered + row0 * RB;
-        const int nunits = nm * V;
-        for (int base = tid; base < nunits; base += NT * UNROLL) {
-            uint4 v[UNROLL];
-            int dst[UNROLL], l_[UNROLL], part_[UNROLL];
-#pragma unroll
-            for (int u = 0; u < UNROLL; ++u) {
-                const int i = base + u * NT;
-                dst[u] = -2;
-                if (i < nunits) {
-                    const int mi = i / V, part = i - mi * V;
-                    const int l = s_mj[mi];
-                    l_[u] = l;
-                    part_[u] = part;
-                    dst[u] = s_src[l];
-                    if (dst[u] >= 0)
-                        v[u] = hs::ld_v4(P.host_rows + (size_t)s_hrow[l] * RB + part * 16);
-                    else
-                        v[u] = make_uint4(0, 0, 0, 0);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < UNROLL; ++u) {
-                if (dst[u] == -2) continue;
-                if (dst[u] >= 0) hs::st_v4(P.rows + (size_t)dst[u] * RB + part_[u] * 16, v[u]);
-                hs::st_v4(gdst + (size_t)l_[u] * RB + part_[u] * 16, v[u]);
-            }
-        }
-        for (int mi = tid; mi < nm; mi += NT) {
-            const int l = s_mj[mi];
-            const int d = s_src[l];
-            resolved[row0 + l] = d;
-            if (fp8) {
-                const float sc = d >= 0 ? P.host_scales[s_hrow[l]] : 0.f;
-                if (d >= 0) P.scales[d] = sc;
-                gscale[row0 + l] = sc;
-            }
-        }
+        hs::cluster_wait();
     }
     if (err) atomicOr(P.err, err);
 }
 
 int pick_cluster(int K) {
-    // 8 CTAs per request (portable cluster size); fewer for short lists
-    int G = 8;
-    while (G > 1 && (K + G - 1) / G < 32) G >>= 1;
-    return G;
+    // one bookkeeping CTA + up to 7 workers (portable cluster size), each
+    // worker owning at least 32 entries
+    int W = 7;
+    while (W > 1 && (K + W - 1) / W < 32) --W;
+    return W + 1;
 }
 
 }  // namespace
 
 size_t hs_resolve_smem_bytes(int K, int G, int C) {
-    (void)C;
-    const int chunk = (K + G - 1) / G;
-    Smem L{chunk, next_pow2(K), K};
+    const int chunk = (K + G - 2) / (G - 1);
+    Smem L{chunk, next_pow2(K), K, C, G - 1};
     return L.total();
 }
 
@@ -397,7 +446,7 @@ hs_status hs_resolve_prepare(hs_pool *pool) {
         const size_t b = hs_resolve_smem_bytes(K, pick_cluster(K), pool->cfg.hot_rows);
         if (b > mx) mx = b;
     }
-    if (mx > 200 * 1024) return HS_ERR_UNSUPPORTED;
+    if (mx > 232448) return HS_ERR_UNSUPPORTED;  // shared memory per block on sm_103
     HS_CUDA_TRY(cudaFuncSetAttribute(resolve_kernel<1152>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx));
     HS_CUDA_TRY(cudaFuncSetAttribute(resolve_kernel<576>,
@@ -409,7 +458,7 @@ hs_status hs_launch_resolve(hs_pool *pool, int32_t B, const int32_t *req_ids, co
                             int32_t K, int32_t *resolved, void *gathered, float *gscale,
                             int32_t *counts, cudaStream_t stream) {
     const int G = pick_cluster(K);
-    const int chunk = (K + G - 1) / G;
+    const int chunk = (K + G - 2) / (G - 1);
     const size_t smem = hs_resolve_smem_bytes(K, G, pool->cfg.hot_rows);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G, B, 1);
