@@ -43,6 +43,23 @@ def _dist():
     return ws, rank, local
 
 
+def max_over_ranks(x: float) -> float:
+    """The largest value over all ranks (CUDA tensor under NCCL, CPU under gloo)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, ms_per_step_max: float) -> float:
+    """Units all ranks processed per second, timed by the slowest rank."""
+    return units_per_rank * world / (ms_per_step_max * 1e-3)
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -269,12 +286,8 @@ def run_gpu(args):
     cnt_sum = counts_acc.cpu().numpy()
     t_res = [evs[s][0].elapsed_time(evs[s][1]) for s in range(steps)]
     t_dec = [evs[s][1].elapsed_time(evs[s][2]) for s in range(steps)]
-    ms_step = (sum(t_res) + sum(t_dec)) / steps
-    if ws > 1:
-        tt = torch.tensor([ms_step], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step = float(tt.item())
-    steps_per_s = ws / (ms_step * 1e-3)
+    ms_step = max_over_ranks((sum(t_res) + sum(t_dec)) / steps)
+    steps_per_s = whole_job_rate(1.0, ws, ms_step)
     res_ms = sum(t_res) / steps
     dec_ms = sum(t_dec) / steps
     rows_per_s = ws * w.B * w.K / (res_ms * 1e-3)

@@ -204,6 +204,13 @@ hs_status hs_sparse_mla_decode_static_ws(hs_pool_t pool, int32_t B, int32_t T, i
                                          const int32_t *d_topk_idx, const int32_t *d_req_ids,
                                          float sm_scale, void *d_out, float *d_lse, void *stream);
 
+/* Failure-detection check: launches one device wait on a barrier phase that
+ * nothing completes, bounded by limit_us (1 .. 2,000,000) exactly like the
+ * decode pipeline's waits. The wait gives up, sets HS_DEVERR_TIMEOUT in the
+ * pool's device error word (read it with hs_pool_get_error) and the kernel
+ * returns, leaving the context usable. Asynchronous on `stream`. */
+hs_status hs_pool_check_bounded_wait(hs_pool_t pool, uint32_t limit_us, void *stream);
+
 /* Human-readable name of a status. */
 const char *hs_status_string(hs_status s);
 

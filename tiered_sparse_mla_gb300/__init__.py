@@ -32,6 +32,7 @@ EXPORTED = [
     "hs_gpu_scales", "hs_host_scales", "hs_pool_snapshot", "hs_pool_restore",
     "hs_pool_get_error", "hs_resolve_topk", "hs_sparse_mla_decode",
     "hs_decode_workspace_bytes", "hs_status_string", "hs_sparse_mla_decode_static_ws",
+    "hs_pool_check_bounded_wait",
 ]
 HS_STATIC_DECODE_WS_BYTES = 24 << 20
 
@@ -94,6 +95,7 @@ def load() -> C.CDLL:
         "hs_sparse_mla_decode_static_ws": ([vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp,
                                             C.c_float, vp, vp, vp], i32),
         "hs_status_string": ([i32], C.c_char_p),
+        "hs_pool_check_bounded_wait": ([vp, C.c_uint32, vp], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -249,6 +251,11 @@ class Pool:
 
     def hot_release(self, req: int):
         _check("hs_hot_release", load().hs_hot_release(self.handle, req))
+
+    def check_bounded_wait(self, limit_us: int, stream=None):
+        """Runs a device wait that nothing completes; it must time out (see hs.h)."""
+        _check("hs_pool_check_bounded_wait",
+               load().hs_pool_check_bounded_wait(self.handle, limit_us, _stream(stream)))
 
     def get_error(self) -> int:
         v = C.c_uint32()

@@ -849,3 +849,25 @@ extern "C" hs_status hs_sparse_mla_decode_static_ws(
                                 d_topk_idx, d_req_ids, sm_scale, d_out, d_lse, g_static_ws[dev],
                                 HS_STATIC_DECODE_WS_BYTES, stream);
 }
+
+// ---------------------------------------------------------------- bounded-wait check
+namespace {
+// One thread waits on an mbarrier phase that nothing completes, with the same
+// bounded wait the decode pipeline uses; it must give up after `limit_ns`.
+__global__ void bounded_wait_check_kernel(uint32_t *err, unsigned long long limit_ns) {
+    __shared__ __align__(8) unsigned long long bar;
+    const uint32_t b = hs::smem_addr(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        fence_mbar_init();
+        if (!mbar_wait(b, 0, limit_ns)) atomicOr(err, HS_DEVERR_TIMEOUT);
+    }
+}
+}  // namespace
+
+extern "C" hs_status hs_pool_check_bounded_wait(hs_pool_t pool, uint32_t limit_us, void *stream) {
+    if (!pool || limit_us == 0 || limit_us > 2000000) return HS_ERR_INVALID_ARG;
+    bounded_wait_check_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        pool->d_err, 1000ull * limit_us);
+    return cudaGetLastError() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+}
