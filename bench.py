@@ -200,6 +200,10 @@ def run_gpu(args):
     w = W.AgentMix() if agent else W.WORKLOADS[name]
     if args.batch and args.batch != w.B:
         w = w.scaled(B=args.batch)
+    if args.ctx and not agent and args.ctx != w.ctx:
+        # a shorter context keeps the decode work (K rows per request) and
+        # shrinks the pool, for profiler captures; not a bench line
+        w = w.scaled(ctx=args.ctx)
     steps = args.steps or DEFAULT_STEPS[name]
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
@@ -321,6 +325,8 @@ def run_gpu(args):
 
     launches = 2 + (1 if hs.hs_decode_workspace_bytes(w.B, w.T, w.H, w.K) > 0 else 0)
     desc = DESCS[name] if (agent or w.B == W.WORKLOADS[name].B) else f"{DESCS[name]} [batch {w.B}]"
+    if not agent and w.ctx != W.WORKLOADS[name].ctx:
+        desc += f" [context {w.ctx}]"
     line = {
         "metric": METRIC, "value": round(steps_per_s, 2), "unit": "decode steps/s",
         "n_gpus": ws, "steps": steps, "warmup": args.warmup,
@@ -524,6 +530,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="requests per step (default: the workload's; smaller only for profiling)")
+    ap.add_argument("--ctx", type=int, default=0,
+                    help="override the context length (profiling captures only)")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(DESCS),
                     help="resident (default, the headline) or another configuration")
     args = ap.parse_args()

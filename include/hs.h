@@ -170,7 +170,8 @@ hs_status hs_resolve_topk(hs_pool_t pool, int32_t B, const int32_t *d_req_ids,
  *   d_lse   float [B][T][H]      = ln sum_j exp(sm_scale * q.k_j); -inf if none valid
  *   d_workspace / ws_bytes: at least hs_decode_workspace_bytes(B, T, H, K)
  *   bytes of device memory, 256-byte aligned (may be NULL when that is 0).
- * Requires H*T <= 128*64 and K >= 1. */
+ * Requires 1 <= T <= 32767, H*T <= 128*65535, B <= 65535 and K >= 1; q, gathered
+ * and out 16-byte aligned. */
 hs_status hs_sparse_mla_decode(hs_pool_t pool, int32_t B, int32_t T, int32_t H, int32_t K,
                                const void *d_q, const void *d_gathered,
                                const float *d_gathered_scale, const int32_t *d_resolved,

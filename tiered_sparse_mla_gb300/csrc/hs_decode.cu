@@ -14,33 +14,50 @@
 // Work unit: (request, 128-row M tile, KV split), run by a cluster of two CTAs.
 // The 576-wide rows are nine 64-column chunks. CTA h (h = 0, 1):
 //   - holds Q for its share of the QK depth (chunks 0-4 for h = 0, 5-8 for
-//     h = 1) and accumulates O for output columns [256h, 256h + 256) (V chunks
-//     0-3 or 4-7); per 64-key tile it therefore loads only chunks 4h..4h+4;
+//     h = 1) in tensor memory and accumulates O for output columns
+//     [256h, 256h + 256) (V chunks 0-3 or 4-7); per 64-key tile it therefore
+//     loads only chunks 4h..4h+4;
 //   - computes a partial S over its depth share into TMEM, sends it (rounded
 //     to f16 after scaling by sm_scale * log2 e) to the peer through
 //     distributed shared memory and adds the peer's partial; both CTAs add
 //     the same two rounded values, so they hold bit-identical S and take
 //     identical softmax decisions;
-//   - runs O_h += P V_h on its own V chunks.
-// Roles inside a CTA (288 threads):
-//   warp 0     TMA producer: Q once, then one 5-chunk tile group per 64 keys,
-//              double-buffered; L2 prefetch of the split's rows at start;
-//   warp 1     MMA issuer (one thread): S_i into one of two TMEM S buffers,
-//              then O += P_{i-1} V_{i-1}; V is read from the same smem chunks
-//              as K through an MN-major descriptor (no transpose stored);
-//   warps 2-3  FP8 only: convert e4m3 chunks in place to f16 with the row
-//              scale folded in, and Q from bf16 to f16 once;
-//   warps 4-7  one thread per query row (TMEM lane): stage the partial S as
-//              f16 of S * sm_scale * log2(e) (the next tile's partial while
-//              this tile's PV runs), add the peer's partial, masking, online
-//              softmax with a conditional rescale (the running max only moves
-//              when a tile's max exceeds it by 2^8), P to smem, epilogue;
-//   warp 8     courier: sends each staged partial to the peer in one bulk
-//              shared-to-shared copy and tells the peer when its partial has
-//              been read, so no softmax warp waits on a cluster-scope release.
-// TMEM: O half 256 columns + 2 x 64 S columns (512 allocated).
+//   - runs O_h += P V_h on its own V chunks, with P in tensor memory.
+// Four tile groups are in flight, and a tile's partial S leaves for the peer
+// two tiles before its softmax, so the exchange overlaps the softmax of the
+// tile in between.
+// Roles inside a CTA (384 threads):
+//   warp 0     TMA producer: Q once, into the space of tile groups 2-3 (their
+//              first loads wait until Q has moved to TMEM), then one 5-chunk
+//              tile group per 64 keys; L2 prefetch of the rows a few tiles
+//              ahead;
+//   warp 1     MMA issuer (one thread): S_j = Q K_j^T into the TMEM S buffer
+//              (A = Q from TMEM) once tile j has landed and S_{j-1} has been
+//              read; O += P_i V_i (A = P from TMEM, V read from the same smem
+//              chunks as K through an MN-major descriptor, no transpose
+//              stored) once P_i is written;
+//   warp 2     per tile: the lowest query token that sees each key (from the
+//              resolved flags, top-K positions and context length) into a
+//              shared ring, so that no softmax warp waits on a global load;
+//              FP8 only: convert e4m3 chunks in place to f16 with the row
+//              scale folded in;
+//   warp 3     courier: sends each staged partial to the peer in one bulk
+//              shared-to-shared copy;
+//   warps 4-7  stagers, one thread per query row (TMEM lane): read S, free it
+//              for the next QK, and write the partial as f16 of
+//              S * sm_scale * log2(e) for the courier;
+//   warps 8-11 softmax, one thread per query row: add the two partials
+//              (then one thread tells the peer its partial has been read),
+//              masking (skipped for tiles every row sees), online softmax
+//              with a conditional rescale (the running max only moves when a
+//              tile's max exceeds it by 2^8), P to TMEM, epilogue.
+// Stagers run up to two tiles ahead of the softmax, so the exchange of a
+// tile's partials overlaps the softmax of the tiles before it.
+// TMEM (512 columns): O half 256 | S 64 | P 32 | Q 160.
 // Every mbarrier wait is bounded in time; on expiry the kernel sets
-// HS_DEVERR_TIMEOUT, drains its own copies and MMAs and returns.
+// HS_DEVERR_TIMEOUT, drains its own copies and MMAs and returns. Roles hand
+// over through mbarriers only, so one that gives up leaves no other waiting
+// on a hardware barrier.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -56,35 +73,44 @@ namespace {
 
 using namespace hs::tc;
 
-constexpr int NTHR = 288;  // 9 warps
+constexpr int NTHR = 384;  // 12 warps
+constexpr int NSTG = 128;  // stager threads (warps 4-7)
+constexpr int NSFT = 128;  // softmax threads (warps 8-11)
 constexpr int BM = 128, BN = 64;
 constexpr int NLC = 5;               // chunks a CTA loads per 64-key tile
-constexpr int NG = 2;                // tile groups in flight
+constexpr int NG = 4;                // tile groups in flight
+constexpr int NQ_MAX = 5;            // Q chunks a CTA holds
 constexpr int QCH_BYTES = BM * 128;  // 128 rows x 64 columns x 2 B
 constexpr int KCH_BYTES = BN * 128;  // 64 keys x 64 columns x 2 B
 constexpr int FCH_BYTES = BN * 64;   // 64 keys x 64 e4m3 codes
-constexpr int P_BYTES = BM * 128;    // 128 rows x 64 keys x 2 B
 constexpr int X_BYTES = BM * 128;    // 128 rows x 64 f16 partial scores
 constexpr float TAU2 = 8.f;          // rescale threshold, log2 units
-constexpr uint32_t TMEM_COLS = 512, TM_O = 0, TM_S = 256;
+constexpr uint32_t TMEM_COLS = 512, TM_O = 0, TM_S = 256, TM_P = 320, TM_Q = 352;
+static_assert(TM_Q + 32 * NQ_MAX <= TMEM_COLS, "tensor memory");
 
 struct Cfg {
-    static constexpr int OFF_Q = 0;
-    static constexpr int OFF_RING = OFF_Q + NLC * QCH_BYTES;
-    static constexpr int OFF_P = OFF_RING + NG * NLC * KCH_BYTES;
-    static constexpr int OFF_XIN = OFF_P + P_BYTES;      // the peer's partial S (f16)
-    static constexpr int OFF_XOUT = OFF_XIN + X_BYTES;   // own partial S (f16), sent to the peer
-    static constexpr int OFF_KPOS = OFF_XOUT + X_BYTES;  // int32 [2][64]
-    static constexpr int OFF_BAR = OFF_KPOS + 2 * BN * 4;
+    static constexpr int OFF_RING = 0;
+    static constexpr int OFF_QSTAGE = OFF_RING + 2 * NLC * KCH_BYTES;  // tile groups 2-3
+    static constexpr int OFF_XIN = OFF_RING + NG * NLC * KCH_BYTES;   // [2] the peer's partial S
+    static constexpr int OFF_XOUT = OFF_XIN + 2 * X_BYTES;            // [2] own partial S
+    static constexpr int OFF_KVIS = OFF_XOUT + 2 * X_BYTES;           // int16 [NG][64]
+    static constexpr int OFF_TDMAX = OFF_KVIS + NG * BN * 2;          // int32 [NG]
+    static constexpr int OFF_BAR = OFF_TDMAX + NG * 4;
     static constexpr int B_QFULL = 0, B_QREADY = 1, B_DRAIN = 2, B_GFULL = 3;
     static constexpr int B_GEMPTY = B_GFULL + NG, B_GLANDED = B_GEMPTY + NG;
-    static constexpr int B_SFULL = B_GLANDED + NG, B_PFULL = B_SFULL + 2;
-    static constexpr int B_PVDONE = B_PFULL + 1, B_XFULL = B_PVDONE + 1, B_XTAKEN = B_XFULL + 1;
-    static constexpr int NBAR = B_XTAKEN + 1;
+    static constexpr int B_SFULL = B_GLANDED + NG, B_SFREE = B_SFULL + 1;
+    static constexpr int B_PFULL = B_SFREE + 1, B_PVDONE = B_PFULL + 1;
+    static constexpr int B_XFULL = B_PVDONE + 1;    // [2] the peer's partial has landed
+    static constexpr int B_XTAKEN = B_XFULL + 2;    // [2] the peer has read what this CTA sent
+    static constexpr int B_STAGED = B_XTAKEN + 2;   // [2] own partial written, ready to send
+    static constexpr int B_READ = B_STAGED + 2;     // [2] both partials of a tile have been read here
+    static constexpr int B_KVIS = B_READ + 2;       // [NG] key visibility of a tile written
+    static constexpr int NBAR = B_KVIS + NG;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // [0] TMEM base, [1] abort flag
     static constexpr int SMEM = OFF_MISC + 16;
     static constexpr int SMEM_ALLOC = SMEM + 1024;       // room to align the base to 1 KiB
-    static_assert(OFF_RING % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles need 1 KiB alignment");
+    static_assert(OFF_QSTAGE % 1024 == 0, "swizzled tiles need 1 KiB alignment");
+    static_assert(NQ_MAX * QCH_BYTES <= (NG - 2) * NLC * KCH_BYTES, "Q staging space");
     static_assert(SMEM_ALLOC <= 232448, "shared memory");
 };
 
@@ -135,6 +161,25 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t a) {
                    "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),  \
                    "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),  \
                    "+r"(r[30]), "+r"(r[31])::"memory")
+// TMEM store of 32 columns of 32-bit words from this thread's lane.
+#define HS_TMEM_ST32(taddr, r)                                                                    \
+    asm volatile(                                                                                 \
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"   \
+        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"      \
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),           \
+        "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),          \
+        "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]),      \
+        "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),      \
+        "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])                               \
+        : "memory")
+
+#define HS_TMEM_ST16(taddr, r)                                                                    \
+    asm volatile(                                                                                 \
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"   \
+        "%13,%14,%15,%16};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]),  \
+        "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]),           \
+        "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])                                           \
+        : "memory")
 
 template <bool FP8>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
@@ -145,6 +190,20 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
         __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
         return *reinterpret_cast<uint32_t *>(&h);
     }
+}
+
+// (float(a.lo) + float(b.lo), float(a.hi) + float(b.hi)) for two f16 pairs.
+// The sum is symmetric in a and b, bit for bit (a -0 that the first add
+// turns into +0 leaves every sum unchanged).
+__device__ __forceinline__ float2 add_f16x2_f32(uint32_t a, uint32_t b) {
+    float2 r;
+    asm("{\n .reg .b16 al, ah, bl, bh;\n .reg .f32 t0, t1;\n"
+        " mov.b32 {al, ah}, %2;\n mov.b32 {bl, bh}, %3;\n"
+        " add.rn.f32.f16 t0, al, 0f00000000;\n add.rn.f32.f16 t1, ah, 0f00000000;\n"
+        " add.rn.f32.f16 %0, bl, t0;\n add.rn.f32.f16 %1, bh, t1;\n}"
+        : "=f"(r.x), "=f"(r.y)
+        : "r"(a), "r"(b));
+    return r;
 }
 
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
@@ -166,11 +225,47 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t n) {
-    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+// One kind::f16 MMA with A from TMEM; the B descriptor comes as two 32-bit
+// halves (only the low half changes between the MMAs of one operand walk) and
+// the accumulate flag is a constant, so that issuing costs a few instructions.
+template <bool ACC>
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint32_t blo, uint32_t bhi,
+                                       uint32_t idesc) {
+    if (ACC)
+        asm volatile(
+            "{\n .reg .b64 bd;\n mov.b64 bd, {%2, %3};\n"
+            " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, 1;\n}\n" ::"r"(d),
+            "r"(a), "r"(blo), "r"(bhi), "r"(idesc)
+            : "memory");
+    else
+        asm volatile(
+            "{\n .reg .b64 bd;\n mov.b64 bd, {%2, %3};\n"
+            " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, 0;\n}\n" ::"r"(d),
+            "r"(a), "r"(blo), "r"(bhi), "r"(idesc)
+            : "memory");
 }
 
-// Row r, 16-byte chunk c of an S exchange buffer (XOR swizzle against bank conflicts).
+// S = Q K^T over NC chunks of the depth: A = Q chunk c at TMEM columns
+// aq + 32 c, B = K chunk c at smem descriptor (blo, bhi) + c * chunk bytes.
+// Straight-line: 4 K steps of 16 per chunk.
+template <int NC>
+__device__ __forceinline__ void issue_qk(uint32_t dS, uint32_t aq, uint32_t blo, uint32_t bhi,
+                                         uint32_t idesc) {
+#pragma unroll
+    for (int c = 0; c < NC; ++c)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t a = aq + 32u * c + 8u * k;
+            const uint32_t lo = blo + (uint32_t)((c * KCH_BYTES + 32 * k) >> 4);
+            if (c == 0 && k == 0)
+                mma_ts<false>(dS, a, lo, bhi, idesc);
+            else
+                mma_ts<true>(dS, a, lo, bhi, idesc);
+        }
+}
+
+// Row r, 16-byte chunk c of a 128-byte-per-row tile with the 128-byte swizzle
+// (the TMA layout of Q, and the layout of the S exchange buffers).
 __device__ __forceinline__ uint32_t x_off(int r, int c) {
     return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
@@ -193,8 +288,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int nq = half ? 4 : 5;      // Q chunks held (global chunks 5h .. 5h+nq-1)
     const int lc0 = half ? 1 : 0;     // first local chunk used by QK (local chunk lc = global 4h+lc)
     volatile int32_t *misc = reinterpret_cast<volatile int32_t *>(smem + C::OFF_MISC);
-    int32_t *kpos = reinterpret_cast<int32_t *>(smem + C::OFF_KPOS);
-    const uint32_t sQ = base + C::OFF_Q, sR = base + C::OFF_RING, sP = base + C::OFF_P;
+    int16_t *kvis = reinterpret_cast<int16_t *>(smem + C::OFF_KVIS);
+    volatile int32_t *tdmax = reinterpret_cast<volatile int32_t *>(smem + C::OFF_TDMAX);
+    const uint32_t sR = base + C::OFF_RING, sQst = base + C::OFF_QSTAGE;
     const uint32_t sXin = base + C::OFF_XIN, sXout = base + C::OFF_XOUT;
     auto bar = [&](int i) { return base + C::OFF_BAR + 8u * (uint32_t)i; };
     auto slot = [&](int g, int lc) { return sR + (uint32_t)((g * NLC + lc) * KCH_BYTES); };
@@ -205,19 +301,24 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::B_QFULL), 1);
-        mbar_init(bar(C::B_QREADY), 64);
+        mbar_init(bar(C::B_QREADY), NSTG + NSFT);
         mbar_init(bar(C::B_DRAIN), 1);
         for (int g = 0; g < NG; ++g) {
-            mbar_init(bar(C::B_GFULL + g), FP8 ? 64 : 1);
+            mbar_init(bar(C::B_GFULL + g), FP8 ? 32 : 1);
             mbar_init(bar(C::B_GEMPTY + g), 1);
             mbar_init(bar(C::B_GLANDED + g), 1);
+            mbar_init(bar(C::B_KVIS + g), 32);
         }
         mbar_init(bar(C::B_SFULL), 1);
-        mbar_init(bar(C::B_SFULL + 1), 1);
-        mbar_init(bar(C::B_PFULL), 128);
+        mbar_init(bar(C::B_SFREE), NSTG);
+        mbar_init(bar(C::B_PFULL), NSFT);
         mbar_init(bar(C::B_PVDONE), 1);
-        mbar_init(bar(C::B_XFULL), 1);   // own arm + the peer's bulk copy bytes
-        mbar_init(bar(C::B_XTAKEN), 1);  // the peer has read what this CTA sent
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(bar(C::B_XFULL + x), 1);  // own arm + the peer's bulk copy bytes
+            mbar_init(bar(C::B_XTAKEN + x), 1);
+            mbar_init(bar(C::B_STAGED + x), NSTG);
+            mbar_init(bar(C::B_READ + x), 1);
+        }
         misc[1] = 0;
         fence_mbar_init();
     }
@@ -237,18 +338,28 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (lane == 0) {
             mbar_expect_tx(bar(C::B_QFULL), nq * QCH_BYTES);
             for (int c = 0; c < nq; ++c)
-                tma_load_3d(sQ + c * QCH_BYTES, &tm_q, 64 * (5 * half + c), mt * BM, b,
+                tma_load_3d(sQst + c * QCH_BYTES, &tm_q, 64 * (5 * half + c), mt * BM, b,
                             bar(C::B_QFULL));
+            // rows of tile t into L2 ahead of its load; the peer CTA reads other
+            // columns of the same rows, so one of the two prefetches
+            auto prefetch_tile = [&](int t) {
+                if (half == 0 && t < ntiles) {
+                    const int j = k0 + t * BN, n = min(BN, k1 - j);
+                    prefetch_l2(p.gathered + ((size_t)b * p.K + j) * p.row_bytes,
+                                (uint32_t)(n * p.row_bytes));
+                }
+            };
             int issued = 0;
             bool ok = true;
             for (int i = 0; i < ntiles && ok; ++i) {
-                if (i == NG && half == 0) {
-                    // the first groups are in flight: stream the rest of this
-                    // split's rows into L2 ahead of their tile loads
-                    for (int t = NG; t < ntiles; ++t) {
-                        const int j = k0 + t * BN, n = min(BN, k1 - j);
-                        prefetch_l2(p.gathered + ((size_t)b * p.K + j) * p.row_bytes,
-                                    (uint32_t)(n * p.row_bytes));
+                if (i == 0)
+                    for (int t = 2; t < NG + 2; ++t) prefetch_tile(t);
+                if (i >= 2) prefetch_tile(i + NG);
+                if (i == 2) {
+                    // tile groups 2-3 hold the staged Q until it has moved to TMEM
+                    if (!mbar_wait(bar(C::B_QREADY), 0)) {
+                        ok = false;
+                        break;
                     }
                 }
                 const int g = i % NG;
@@ -275,100 +386,116 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t AB = FP8 ? 0u : 1u;
-            constexpr uint32_t ID_QK = idesc_f16(AB, 0, BM, BN);
-            constexpr uint32_t ID_PV = idesc_f16(AB, 1, BM, 256);
-            bool ok = mbar_wait(bar(FP8 ? C::B_QREADY : C::B_QFULL), 0);
+            constexpr uint32_t ID_QK = idesc_f16(FP8 ? 0u : 1u, 0, BM, BN);
+            constexpr uint32_t ID_PV = idesc_f16(FP8 ? 0u : 1u, 1, BM, 256);
+            bool ok = mbar_wait(bar(C::B_QREADY), 0);
             tc_fence_after();
-            for (int i = 0; i <= ntiles && ok; ++i) {
-                if (i < ntiles) {
-                    const int g = i % NG;
-                    if (!mbar_wait(bar(C::B_GFULL + g), (uint32_t)(i / NG) & 1u)) {
-                        ok = false;
-                        break;
-                    }
+            // Order QK_0, QK_1, QK_2, then PV_i, QK_{i+3}: the softmax threads
+            // release P_i at about the time the stagers, two tiles ahead, free
+            // S_{i+2}, so each wait is short and suspends instead of spinning.
+            for (int i = -3; i < ntiles && ok; ++i) {
+                if (i >= 0) {
+                    ok = mbar_wait(bar(C::B_PFULL), (uint32_t)i & 1u) && !misc[1];
+                    if (!ok) break;
+                    // O[128 x 256] += P_i[128 x 64] V_i[64 x 256]; frees tile group i % NG
                     tc_fence_after();
-                    const uint32_t dS = tmem + TM_S + (uint32_t)(i & 1) * BN;
-                    // descriptors advance by (bytes >> 4) in their low bits
-                    const uint64_t a0 = desc_sw128(sQ, 16, 1024);
-                    const uint64_t b0 = desc_sw128(slot(g, lc0), 16, 1024);
-                    for (int lc = lc0; lc < NLC; ++lc) {
-                        const uint64_t ac = a0 + (uint64_t)(((lc - lc0) * QCH_BYTES) >> 4);
-                        const uint64_t bc = b0 + (uint64_t)(((lc - lc0) * KCH_BYTES) >> 4);
+                    const uint64_t vb = desc_sw128(slot(i % NG, 0), KCH_BYTES, 1024);
+                    const uint32_t lo = (uint32_t)vb, hi = (uint32_t)(vb >> 32);
+                    if (i == 0)
+                        mma_ts<false>(tmem + TM_O, tmem + TM_P, lo, hi, ID_PV);
+                    else
+                        mma_ts<true>(tmem + TM_O, tmem + TM_P, lo, hi, ID_PV);
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            mma_f16(dS, ac + 2 * k, bc + 2 * k, ID_QK, (lc > lc0) || (k > 0));
-                    }
-                    mma_commit(bar(C::B_SFULL + (i & 1)));
-                }
-                if (i >= 1) {
-                    const int j = i - 1, g = j % NG;
-                    if (!mbar_wait(bar(C::B_PFULL), (uint32_t)j & 1u)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint64_t pa = desc_sw128(sP, 16, 1024);
-                    const uint64_t vb = desc_sw128(slot(g, 0), KCH_BYTES, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)  // O[128 x 256] += P[:, 16kk..] V[16kk.., 0..256)
-                        mma_f16(tmem + TM_O, pa + 2 * kk, vb + 128 * kk, ID_PV, (j > 0) || (kk > 0));
-                    mma_commit(bar(C::B_GEMPTY + g));
+                    for (int kk = 1; kk < 4; ++kk)  // 16 keys = 2048 bytes of V per step
+                        mma_ts<true>(tmem + TM_O, tmem + TM_P + 8u * kk, lo + 128u * kk, hi, ID_PV);
+                    mma_commit(bar(C::B_GEMPTY + i % NG));
                     mma_commit(bar(C::B_PVDONE));
                 }
-                if (misc[1]) ok = false;
+                const int j = i + 3;
+                if (j < ntiles) {
+                    // tile j landed and S_{j-1} read by the stagers
+                    ok = mbar_wait(bar(C::B_GFULL + j % NG), (uint32_t)(j / NG) & 1u) &&
+                         (j == 0 || mbar_wait(bar(C::B_SFREE), (uint32_t)(j - 1) & 1u)) && !misc[1];
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t b0 = desc_sw128(slot(j % NG, lc0), 16, 1024);
+                    if (half)
+                        issue_qk<4>(tmem + TM_S, tmem + TM_Q, (uint32_t)b0, (uint32_t)(b0 >> 32), ID_QK);
+                    else
+                        issue_qk<5>(tmem + TM_S, tmem + TM_Q, (uint32_t)b0, (uint32_t)(b0 >> 32), ID_QK);
+                    mma_commit(bar(C::B_SFULL));
+                }
             }
             if (!ok) fail();
             // every MMA issued above has finished before TMEM and smem are released
             mma_commit(bar(C::B_DRAIN));
             mbar_wait(bar(C::B_DRAIN), 0);
         }
-    } else if (warp < 4) {
-        // ------------------------------------------------------------ FP8 converters
-        if (FP8) {
-            const int ct = threadIdx.x - 64;  // 0..63: one key row of every chunk
-            bool ok = mbar_wait(bar(C::B_QFULL), 0);
-            if (ok) {
-                for (int q = ct; q < nq * QCH_BYTES / 16; q += 64) {
-                    const uint4 v = ld_shared_v4(sQ + q * 16);
-                    st_shared_v4(sQ + q * 16, bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y),
-                                 bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
-                }
-                fence_proxy_async();
-            } else {
-                fail();
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ key visibility, FP8 converter
+        // Key j of a tile is seen by query token t iff its position is at most
+        // L - T + t: store d = clamp(position - (L - T), 0, T), and d = T (seen
+        // by none) for unresolved or absent entries; row t then masks d > t.
+        const int r = p.req_ids[b];
+        const long long first = (long long)((r >= 0 && r < p.max_req) ? p.ctx[r] : 0) - p.T;
+        const int32_t *res_b = p.resolved + (size_t)b * p.K;
+        const int32_t *top_b = p.topk + (size_t)b * p.K;
+        const float *gs = FP8 ? p.gscale + (size_t)b * p.K : nullptr;
+        bool ok = true;
+        for (int i = 0; i < ntiles; ++i) {
+            const int g = i % NG;
+            const uint32_t ph = (uint32_t)(i / NG) & 1u;
+            // the slot's previous tile is finished (FP8: and this tile has landed)
+            if (ok)
+                ok = mbar_wait(bar(FP8 ? C::B_GLANDED + g : C::B_GEMPTY + g), FP8 ? ph : ph ^ 1u) &&
+                     !misc[1];
+            int res[2], top[2];
+            float sc[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // keys lane and lane + 32; loads issued together
+                const int j = k0 + i * BN + lane + 32 * h;
+                const bool in = j < k1;
+                res[h] = in ? res_b[j] : -1;
+                top[h] = in ? top_b[j] : 0;
+                sc[h] = (FP8 && j < p.K) ? gs[j] : 0.f;
             }
-            mbar_arrive(bar(C::B_QREADY));
-            const float *gs = p.gscale + (size_t)b * p.K;
-            for (int i = 0; i < ntiles; ++i) {
-                const int g = i % NG;
-                if (ok) ok = mbar_wait(bar(C::B_GLANDED + g), (uint32_t)(i / NG) & 1u) && !misc[1];
-                const int j = k0 + i * BN + ct;
-                const __half2 s2 = __float2half2_rn(j < p.K ? gs[j] : 0.f);
+            if (FP8) {
+                __half2 s2[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) s2[h] = __float2half2_rn(sc[h]);
                 for (int lc = 0; lc < NLC; ++lc) {
                     // the e4m3 codes sit in the upper half of the slot; every row
                     // is read before any f16 row (which may overlap them) is written
                     const uint32_t sl = slot(g, lc);
-                    uint4 raw4[4];
+                    uint4 raw4[2][4];
                     if (ok) {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            raw4[q] = ld_shared_v4(sl + (KCH_BYTES - FCH_BYTES) + ct * 64 + 16 * q);
+                        for (int h = 0; h < 2; ++h)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                raw4[h][q] = ld_shared_v4(sl + (KCH_BYTES - FCH_BYTES) +
+                                                          (lane + 32 * h) * 64 + 16 * q);
                     }
-                    named_bar_sync(4, 64);  // converter warps only (ids 1-3 belong to softmax + courier)
+                    __syncwarp();
                     if (!ok) continue;
-                    const uint32_t dst = sl + ct * 128;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {  // 16 codes -> 16 f16 = two 16-byte chunks
-                        const uint32_t w[4] = {raw4[q].x, raw4[q].y, raw4[q].z, raw4[q].w};
-                        uint32_t h[8];
+                    for (int h = 0; h < 2; ++h) {
+                        const int ct = lane + 32 * h;
+                        const uint32_t dst = sl + ct * 128;
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            h[2 * e] = hmul2_u32(e4m3x2_to_f16x2(w[e] & 0xffffu), s2);
-                            h[2 * e + 1] = hmul2_u32(e4m3x2_to_f16x2(w[e] >> 16), s2);
+                        for (int q = 0; q < 4; ++q) {  // 16 codes -> 16 f16 = two 16-byte chunks
+                            const uint32_t w[4] = {raw4[h][q].x, raw4[h][q].y, raw4[h][q].z,
+                                                   raw4[h][q].w};
+                            uint32_t hv[8];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                hv[2 * e] = hmul2_u32(e4m3x2_to_f16x2(w[e] & 0xffffu), s2[h]);
+                                hv[2 * e + 1] = hmul2_u32(e4m3x2_to_f16x2(w[e] >> 16), s2[h]);
+                            }
+                            st_shared_v4(dst + (((2 * q) ^ (ct & 7)) << 4), hv[0], hv[1], hv[2], hv[3]);
+                            st_shared_v4(dst + (((2 * q + 1) ^ (ct & 7)) << 4), hv[4], hv[5], hv[6],
+                                         hv[7]);
                         }
-                        st_shared_v4(dst + (((2 * q) ^ (ct & 7)) << 4), h[0], h[1], h[2], h[3]);
-                        st_shared_v4(dst + (((2 * q + 1) ^ (ct & 7)) << 4), h[4], h[5], h[6], h[7]);
                     }
                 }
                 if (ok) {
@@ -376,227 +503,273 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     mbar_arrive(bar(C::B_GFULL + g));
                 }
             }
+            int dm = 0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                long long d = (long long)top[h] - first;
+                d = d < 0 ? 0 : (d > p.T ? p.T : d);
+                const int v = res[h] >= 0 ? (int)d : p.T;
+                dm = max(dm, v);
+                if (ok) kvis[g * BN + lane + 32 * h] = (int16_t)v;
+            }
+            // the largest d of the tile: rows with t >= it skip the mask
+            dm = __reduce_max_sync(0xffffffffu, dm);
+            if (ok && lane == 0) tdmax[g] = dm;
+            mbar_arrive(bar(C::B_KVIS + g));
+        }
+        if (!ok) fail();
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ courier
+        // Sends each staged partial to the peer, in tile order, and arms this
+        // CTA's barrier for the peer's partial of the same tile.
+        if (lane == 0) {
+            const uint32_t peer_xin = hs::dsmem_map(smem + C::OFF_XIN, peer);
+            const uint32_t peer_xfull = hs::dsmem_map(smem + C::OFF_BAR + 8 * C::B_XFULL, peer);
+            bool ok = true;
+            auto send = [&](int j) {
+                const uint32_t x = (uint32_t)(j & 1);
+                if (ok) ok = mbar_wait(bar(C::B_STAGED + x), (uint32_t)(j >> 1) & 1u);
+                if (ok && !misc[1]) {
+                    mbar_expect_tx(bar(C::B_XFULL + x), X_BYTES);  // arms this CTA's receive of tile j
+                    asm volatile(
+                        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes"
+                        " [%0], [%1], %2, [%3];" ::"r"(peer_xin + x * X_BYTES),
+                        "r"(sXout + x * X_BYTES), "r"((uint32_t)X_BYTES), "r"(peer_xfull + 8u * x)
+                        : "memory");
+                }
+            };
+            for (int j = 0; j < ntiles; ++j) send(j);
             if (!ok) fail();
         }
-    } else if (warp == 8) {
-        // ------------------------------------------------------------ courier
-        // Sends each staged partial to the peer and tells the peer when its
-        // data has been read, so that the softmax warps never wait on the
-        // release of a cluster-scope arrive. Mirrors the softmax loop's
-        // barrier sequence: staged(0), then per tile: read(i), staged(i+1).
-        const uint32_t peer_xin = hs::dsmem_map(smem + C::OFF_XIN, peer);
-        const uint32_t peer_xfull = hs::dsmem_map(smem + C::OFF_BAR + 8 * C::B_XFULL, peer);
-        const uint32_t peer_xtaken = hs::dsmem_map(smem + C::OFF_BAR + 8 * C::B_XTAKEN, peer);
-        auto send = [&]() {
-            if (lane == 0 && !misc[1]) {
-                mbar_expect_tx(bar(C::B_XFULL), X_BYTES);  // this CTA's next receive
-                asm volatile(
-                    "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes"
-                    " [%0], [%1], %2, [%3];" ::"r"(peer_xin),
-                    "r"(sXout), "r"((uint32_t)X_BYTES), "r"(peer_xfull)
-                    : "memory");
-            }
-        };
-        if (ntiles > 0) {
-            named_bar_sync(3, 160);
-            send();
-        }
-        for (int i = 0; i < ntiles; ++i) {
-            named_bar_sync(2, 160);
-            if (lane == 0 && !misc[1]) mbar_arrive_remote(peer_xtaken);
-            if (i + 1 < ntiles) {
-                named_bar_sync(3, 160);
-                send();
-            }
-        }
     } else {
-        // ------------------------------------------------------------ softmax + epilogue
-        const int wq = warp - 4;
+        // ------------------------------------------------------------ stagers and softmax
+        // Thread row = TMEM lane (warp w reaches lanes 32 (w % 4) .. + 31).
+        const bool stager = warp < 8;
+        const int wq = warp & 3;
         const int row = wq * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-        const int mg = mt * BM + row;
-        const bool vrow = mg < p.M;
-        const int r = p.req_ids[b];
-        const int L = (r >= 0 && r < p.max_req) ? p.ctx[r] : 0;
-        const int t = vrow ? mg / p.H : 0;
-        const int pos = L - p.T + t;
-        const int32_t *res_b = p.resolved + (size_t)b * p.K;
-        const int32_t *top_b = p.topk + (size_t)b * p.K;
-        // position of key `idx` of this split; INT_MAX for unresolved or absent entries
-        auto key_pos = [&](int idx) {
-            const int j = k0 + idx;
-            return (j < k1 && res_b[j] >= 0) ? top_b[j] : INT_MAX;
-        };
-        if (row < BN) kpos[row] = key_pos(row);
-        named_bar_sync(1, 128);
-        float m2 = -INFINITY, l = 0.f;
-        bool ok = true;
-        // Partial scores travel as f16 of S * sm_scale * log2(e); both CTAs add
-        // the same two rounded values, so their sums are bit-identical.
-        uint32_t own[32];  // this CTA's partial for the tile being sent / processed
-        // Stage tile `i`: read the partial from TMEM, keep it packed, write it
-        // to X_out and (one thread) send it to the peer. Every thread of the
-        // softmax group calls this the same number of times (named barrier).
-        auto stage = [&](int i) {
-            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SFULL + (i & 1)), (i >> 1) & 1));
-            // X_out still holds tile i-1 until the peer has taken it
-            if (ok && i > 0)
-                ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar(C::B_XTAKEN), (i - 1) & 1));
-            if (ok) {
-                tc_fence_after();
-                uint32_t ra[32], rb[32];
-                const uint32_t tS = tmem + lane_off + TM_S + (uint32_t)(i & 1) * BN;
-                HS_TMEM_LD32(tS, ra);
-                HS_TMEM_LD32(tS + 32, rb);
-                HS_TMEM_WAIT_LD32(ra);
-                HS_TMEM_WAIT_LD32(rb);
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_QFULL), 0));
+        if (ok) {
+            // this thread's row of staged Q chunks into its TMEM lane: stagers
+            // even chunks, softmax threads odd ones
+            for (int c = stager ? 0 : 1; c < nq; c += 2) {
+                uint32_t q[32];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    own[e] = pack2<true>(__uint_as_float(ra[2 * e]) * p.scale_log2,
-                                         __uint_as_float(ra[2 * e + 1]) * p.scale_log2);
-                    own[16 + e] = pack2<true>(__uint_as_float(rb[2 * e]) * p.scale_log2,
-                                              __uint_as_float(rb[2 * e + 1]) * p.scale_log2);
+                for (int u = 0; u < 8; ++u) {
+                    const uint4 v = ld_shared_v4(sQst + c * QCH_BYTES + x_off(row, u));
+                    q[4 * u] = FP8 ? bf16x2_to_f16x2(v.x) : v.x;
+                    q[4 * u + 1] = FP8 ? bf16x2_to_f16x2(v.y) : v.y;
+                    q[4 * u + 2] = FP8 ? bf16x2_to_f16x2(v.z) : v.z;
+                    q[4 * u + 3] = FP8 ? bf16x2_to_f16x2(v.w) : v.w;
                 }
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    st_shared_v4(sXout + x_off(row, c), own[4 * c], own[4 * c + 1], own[4 * c + 2],
-                                 own[4 * c + 3]);
-                fence_proxy_async();
+                HS_TMEM_ST32(tmem + lane_off + TM_Q + 32u * (uint32_t)c, q);
             }
-            named_bar_arrive(3, 160);  // staged: the courier warp sends it
-        };
-        if (ntiles > 0) stage(0);
-        // Every softmax thread runs every iteration and reaches every named
-        // barrier (those are not bounded in time); after a failed wait the
-        // remaining work is skipped.
-        for (int i = 0; i < ntiles; ++i) {
-            const int kp_next = (row < BN && i + 1 < ntiles) ? key_pos((i + 1) * BN + row) : INT_MAX;
-            float s[64];
-            if (ok) ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar(C::B_XFULL), i & 1));
-            if (ok) {
+            tmem_wait_st();
+        }
+        fence_proxy_async();  // the staging space is refilled by TMA next
+        tc_fence_before();
+        mbar_arrive(bar(C::B_QREADY));
+
+        if (stager) {
+            // ------------------------------------------------ stagers
+            // Tile j: read the partial S from TMEM, free S, and write it as
+            // f16 of S * sm_scale * log2(e) to X_out[j & 1] once tile j - 2 is
+            // done with that buffer (read here and taken by the peer).
+            for (int j = 0; j < ntiles; ++j) {
+                const uint32_t x = (uint32_t)(j & 1);
+                uint32_t pk[32];
+                if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SFULL), (uint32_t)j & 1u));
+                if (ok) {
+                    tc_fence_after();
+                    uint32_t ra[32], rb[32];
+                    HS_TMEM_LD32(tmem + lane_off + TM_S, ra);
+                    HS_TMEM_LD32(tmem + lane_off + TM_S + 32, rb);
+                    HS_TMEM_WAIT_LD32(ra);
+                    HS_TMEM_WAIT_LD32(rb);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint4 v = ld_shared_v4(sXin + x_off(row, c));
-                    const uint32_t pw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&own[4 * c + e]));
-                        const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&pw[e]));
-                        s[8 * c + 2 * e] = a.x + b.x;
-                        s[8 * c + 2 * e + 1] = a.y + b.y;
+                    for (int e = 0; e < 16; ++e) {
+                        pk[e] = pack2<true>(__uint_as_float(ra[2 * e]) * p.scale_log2,
+                                            __uint_as_float(ra[2 * e + 1]) * p.scale_log2);
+                        pk[16 + e] = pack2<true>(__uint_as_float(rb[2 * e]) * p.scale_log2,
+                                                 __uint_as_float(rb[2 * e + 1]) * p.scale_log2);
                     }
                 }
-            }
-            named_bar_arrive(2, 160);  // X_in read: the courier tells the peer
-            if (ok) {
-                const uint32_t kpa = hs::smem_addr(kpos + (i & 1) * BN);
-#pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const uint4 kv = ld_shared_v4(kpa + 16 * q);
-                    s[4 * q] = (int)kv.x <= pos ? s[4 * q] : -INFINITY;
-                    s[4 * q + 1] = (int)kv.y <= pos ? s[4 * q + 1] : -INFINITY;
-                    s[4 * q + 2] = (int)kv.z <= pos ? s[4 * q + 2] : -INFINITY;
-                    s[4 * q + 3] = (int)kv.w <= pos ? s[4 * q + 3] : -INFINITY;
+                tc_fence_before();
+                mbar_arrive(bar(C::B_SFREE));  // QK of tile j + 1 may overwrite S
+                if (ok && j >= 2) {
+                    const uint32_t ph = (uint32_t)((j - 2) >> 1) & 1u;
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_READ + x), ph) &&
+                                                     mbar_wait(bar(C::B_XTAKEN + x), ph));
                 }
-                // P and O are free once PV of the previous tile has finished
-                if (i > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_PVDONE), (i - 1) & 1));
-            }
-            if (ok) {
-                tc_fence_after();
-                float tmax = -INFINITY;
+                if (ok) {
+                    const uint32_t xo = sXout + x * X_BYTES;
 #pragma unroll
-                for (int j = 0; j < 64; ++j) tmax = fmaxf(tmax, s[j]);
-                if (i == 0) {
-                    m2 = tmax;
-                } else {
-                    const bool need = tmax > m2 + TAU2;
-                    if (__any_sync(0xffffffffu, need)) {
-                        const float alpha = need ? exp2f(m2 - tmax) : 1.f;
-                        if (need) {
-                            l *= alpha;
-                            m2 = tmax;
+                    for (int c = 0; c < 8; ++c)
+                        st_shared_v4(xo + x_off(row, c), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                                     pk[4 * c + 3]);
+                    fence_proxy_async();  // the courier's bulk copy reads it
+                }
+                mbar_arrive(bar(C::B_STAGED + x));
+            }
+        } else {
+            // ------------------------------------------------ softmax, PV, epilogue
+            const int mg = mt * BM + row;
+            const bool vrow = mg < p.M;
+            const int t = vrow ? mg / p.H : 0;  // query token of this row
+            const uint32_t peer_xtaken = hs::dsmem_map(smem + C::OFF_BAR + 8 * C::B_XTAKEN, peer);
+            float m2 = -INFINITY, l = 0.f;
+            // Every softmax thread runs every iteration and reaches every named
+            // barrier (those are not bounded in time); after a failed wait the
+            // remaining work is skipped.
+            for (int i = 0; i < ntiles; ++i) {
+                const uint32_t x = (uint32_t)(i & 1);
+                const int g = i % NG;
+                float s[64];
+                if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_XFULL + x), (i >> 1) & 1));
+                if (ok) {
+                    // S = own partial + the peer's partial, both as sent
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 a = ld_shared_v4(sXout + x * X_BYTES + x_off(row, c));
+                        const uint4 v = ld_shared_v4(sXin + x * X_BYTES + x_off(row, c));
+                        const float2 s0 = add_f16x2_f32(a.x, v.x), s1 = add_f16x2_f32(a.y, v.y);
+                        const float2 s2 = add_f16x2_f32(a.z, v.z), s3 = add_f16x2_f32(a.w, v.w);
+                        s[8 * c] = s0.x;
+                        s[8 * c + 1] = s0.y;
+                        s[8 * c + 2] = s1.x;
+                        s[8 * c + 3] = s1.y;
+                        s[8 * c + 4] = s2.x;
+                        s[8 * c + 5] = s2.y;
+                        s[8 * c + 6] = s3.x;
+                        s[8 * c + 7] = s3.y;
+                    }
+                }
+                // X_in[x] and X_out[x] read by every softmax thread: one thread
+                // frees X_out[x] for the stagers and X_in[x] for the peer
+                named_bar_sync(2, NSFT);
+                if (threadIdx.x == 256) {
+                    mbar_arrive(bar(C::B_READ + x));
+                    mbar_arrive_peer(peer_xtaken + 8u * x);
+                }
+                if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_KVIS + g), (uint32_t)(i / NG) & 1u));
+                uint32_t pk[32];
+                float alpha = 1.f;
+                bool need = false;
+                if (ok) {
+                    if (!__all_sync(0xffffffffu, tdmax[g] <= t)) {
+                        // some key of this tile is hidden from some row of this warp
+                        const uint32_t ka = hs::smem_addr(kvis + g * BN);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {  // 8 keys per 16 bytes, lower key in the low half
+                            const uint4 kv = ld_shared_v4(ka + 16 * q);
+                            const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int d0 = (int)(w[e] & 0xffffu), d1 = (int)(w[e] >> 16);
+                                s[8 * q + 2 * e] = d0 <= t ? s[8 * q + 2 * e] : -INFINITY;
+                                s[8 * q + 2 * e + 1] = d1 <= t ? s[8 * q + 2 * e + 1] : -INFINITY;
+                            }
                         }
+                    }
+                    // tree reductions: no long dependency chains
+                    float mx[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        mx[e] = fmaxf(fmaxf(s[e], s[e + 16]), fmaxf(s[e + 32], s[e + 48]));
+#pragma unroll
+                    for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+                        for (int e = 0; e < w; ++e) mx[e] = fmaxf(mx[e], mx[e + w]);
+                    const float tmax = mx[0];
+                    if (i == 0) {
+                        m2 = tmax;
+                    } else if (tmax > m2 + TAU2) {
+                        need = true;
+                        alpha = exp2f(m2 - tmax);
+                        l *= alpha;
+                        m2 = tmax;
+                    }
+                    const float mref = (m2 == -INFINITY) ? 0.f : m2;
+                    float ls[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ls[e] = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float a = exp2f(s[2 * e] - mref), c = exp2f(s[2 * e + 1] - mref);
+                        ls[e & 7] += a + c;
+                        pk[e] = pack2<FP8>(a, c);
+                    }
+                    l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+                    // P and O are free once PV of the previous tile has finished
+                    if (i > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_PVDONE), (uint32_t)(i - 1) & 1u));
+                }
+                if (ok) {
+                    tc_fence_after();
+                    HS_TMEM_ST32(tmem + lane_off + TM_P, pk);
+                    if (__any_sync(0xffffffffu, need)) {
 #pragma unroll 1
                         for (int cc = 0; cc < 8; ++cc) {
                             uint32_t o[32];
                             const uint32_t tO = tmem + lane_off + TM_O + 32 * cc;
                             HS_TMEM_LD32(tO, o);
                             HS_TMEM_WAIT_LD32(o);
-                            float f[32];
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(o[e]) * alpha;
-                            tmem_st32(tO, f);
+                            for (int e = 0; e < 32; ++e)
+                                o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            HS_TMEM_ST32(tO, o);
                         }
-                        tmem_wait_st();
                     }
+                    tmem_wait_st();
                 }
-                const float mref = (m2 == -INFINITY) ? 0.f : m2;
-                float lsum = 0.f;
-                uint32_t pk[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float a = exp2f(s[2 * e] - mref), c = exp2f(s[2 * e + 1] - mref);
-                    lsum += a + c;
-                    pk[e] = pack2<FP8>(a, c);
-                }
-                l += lsum;
-                const uint32_t prow = sP + row * 128;
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    st_shared_v4(prow + ((q ^ (row & 7)) << 4), pk[4 * q], pk[4 * q + 1],
-                                 pk[4 * q + 2], pk[4 * q + 3]);
-                fence_proxy_async();
                 tc_fence_before();
-                mbar_arrive(bar(C::B_PFULL));
+                mbar_arrive(bar(C::B_PFULL));  // P_i (and a rescaled O) complete in TMEM
             }
-            // the next tile's exchange overlaps this tile's PV
-            if (i + 1 < ntiles) stage(i + 1);
-            if (row < BN && i + 1 < ntiles) kpos[((i + 1) & 1) * BN + row] = kp_next;
-        }
-        if (ok && ntiles > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_PVDONE), (ntiles - 1) & 1));
-            tc_fence_after();
-        }
-        if (!ok) fail();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        const size_t orow = (size_t)b * p.M + mg;
-        if (ok) {
+            if (ok && ntiles > 0) {
+                // the last PV's completion covers every earlier one
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_PVDONE), (uint32_t)(ntiles - 1) & 1u));
+                tc_fence_after();
+            }
+            if (!ok) fail();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const size_t orow = (size_t)b * p.M + mg;
+            if (ok) {
 #pragma unroll 1
-            for (int cc = 0; cc < 8; ++cc) {
-                uint32_t o[32];
-                HS_TMEM_LD32(tmem + lane_off + TM_O + 32 * cc, o);
-                HS_TMEM_WAIT_LD32(o);
-                if (!vrow) continue;
-                const int col = half * 256 + 32 * cc;
-                if (p.nsplit == 1) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * 512 + col);
+                for (int cc = 0; cc < 8; ++cc) {
+                    uint32_t o[32];
+                    HS_TMEM_LD32(tmem + lane_off + TM_O + 32 * cc, o);
+                    HS_TMEM_WAIT_LD32(o);
+                    if (!vrow) continue;
+                    const int col = half * 256 + 32 * cc;
+                    if (p.nsplit == 1) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * 512 + col);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t w[4];
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t w[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            w[e] = pack2<false>(__uint_as_float(o[8 * q + 2 * e]) * inv,
-                                                __uint_as_float(o[8 * q + 2 * e + 1]) * inv);
-                        dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+                            for (int e = 0; e < 4; ++e)
+                                w[e] = pack2<false>(__uint_as_float(o[8 * q + 2 * e]) * inv,
+                                                    __uint_as_float(o[8 * q + 2 * e + 1]) * inv);
+                            dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    } else {
+                        float4 *dst = reinterpret_cast<float4 *>(
+                            p.ws_o + (((size_t)split * p.B + b) * p.M + mg) * 512 + col);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            dst[q] = make_float4(__uint_as_float(o[4 * q]) * inv,
+                                                 __uint_as_float(o[4 * q + 1]) * inv,
+                                                 __uint_as_float(o[4 * q + 2]) * inv,
+                                                 __uint_as_float(o[4 * q + 3]) * inv);
                     }
-                } else {
-                    float4 *dst = reinterpret_cast<float4 *>(
-                        p.ws_o + (((size_t)split * p.B + b) * p.M + mg) * 512 + col);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        dst[q] = make_float4(__uint_as_float(o[4 * q]) * inv,
-                                             __uint_as_float(o[4 * q + 1]) * inv,
-                                             __uint_as_float(o[4 * q + 2]) * inv,
-                                             __uint_as_float(o[4 * q + 3]) * inv);
                 }
             }
-        }
-        if (vrow && half == 0) {
-            const float lse = (ok && l > 0.f) ? (m2 + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-            if (p.nsplit == 1)
-                p.lse[orow] = lse;
-            else
-                p.ws_lse[((size_t)split * p.B + b) * p.M + mg] = lse;
+            if (vrow && half == 0) {
+                const float lse = (ok && l > 0.f) ? (m2 + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+                if (p.nsplit == 1)
+                    p.lse[orow] = lse;
+                else
+                    p.ws_lse[((size_t)split * p.B + b) * p.M + mg] = lse;
+            }
         }
     }
 
@@ -754,7 +927,8 @@ extern "C" hs_status hs_sparse_mla_decode(hs_pool_t pool, int32_t B, int32_t T, 
                                           void *d_workspace, size_t ws_bytes, void *stream) {
     if (!pool || !d_q || !d_gathered || !d_resolved || !d_topk_idx || !d_req_ids || !d_out || !d_lse)
         return HS_ERR_INVALID_ARG;
-    if (B < 0 || T < 1 || H < 1 || K < 1 || B > 65535 || (int64_t)T * H > (int64_t)BM * 65535)
+    if (B < 0 || T < 1 || T > 32767 || H < 1 || K < 1 || B > 65535 ||
+        (int64_t)T * H > (int64_t)BM * 65535)
         return HS_ERR_INVALID_ARG;
     const bool fp8 = pool->cfg.dtype == HS_FP8_E4M3_ROWSCALE;
     if (fp8 != (d_gathered_scale != nullptr)) return HS_ERR_INVALID_ARG;

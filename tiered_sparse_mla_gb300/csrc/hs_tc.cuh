@@ -37,18 +37,32 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Non-blocking test: has the phase with the given parity completed?
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Waits for the phase with the given parity to complete. Gives up after
 // `limit_ns` of wall time (returns false) so that a broken pipeline cannot
-// hang the GPU.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          uint64_t limit_ns = 2000000000ull) {
-    if (mbar_try(bar, parity)) return true;
+// hang the GPU. The polling loop is out of line: call sites stay small.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                                   uint64_t limit_ns) {
     const uint64_t t0 = globaltimer();
     for (;;) {
         for (int i = 0; i < 64; ++i)
             if (mbar_try(bar, parity)) return true;
         if (globaltimer() - t0 > limit_ns) return false;
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint64_t limit_ns = 2000000000ull) {
+    return mbar_try(bar, parity) || mbar_wait_slow(bar, parity, limit_ns);
 }
 
 // Cluster-scope variants: waits that acquire what a peer CTA released, and an
@@ -63,15 +77,23 @@ __device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) 
         : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
-                                                  uint64_t limit_ns = 2000000000ull) {
-    if (mbar_try_cluster(bar, parity)) return true;
+static __device__ __noinline__ bool mbar_wait_cluster_slow(uint32_t bar, uint32_t parity,
+                                                           uint64_t limit_ns) {
     const uint64_t t0 = globaltimer();
     for (;;) {
         for (int i = 0; i < 64; ++i)
             if (mbar_try_cluster(bar, parity)) return true;
         if (globaltimer() - t0 > limit_ns) return false;
     }
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns = 2000000000ull) {
+    return mbar_try_cluster(bar, parity) || mbar_wait_cluster_slow(bar, parity, limit_ns);
+}
+// Arrive on a peer CTA's barrier with the default (CTA-scope) release: for
+// hand-overs whose data moves by bulk copies that signal their own barrier.
+__device__ __forceinline__ void mbar_arrive_peer(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
@@ -190,6 +212,17 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// The same MMA with the A operand read from tensor memory: M rows in lanes
+// 0..M-1, two consecutive 16-bit K elements per 32-bit column (the lower K
+// index in the low half), so one K = 16 step spans 8 columns.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 // Arrives on `bar` once every tcgen05.mma issued so far by this thread is done.
