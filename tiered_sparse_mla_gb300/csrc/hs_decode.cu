@@ -29,8 +29,9 @@
 // Roles inside a CTA (384 threads):
 //   warp 0     TMA producer: Q once, into the space of tile groups 2-3 (their
 //              first loads wait until Q has moved to TMEM), then one 5-chunk
-//              tile group per 64 keys; L2 prefetch of the rows a few tiles
-//              ahead;
+//              tile group per 64 keys (no L2 prefetch: with four groups in
+//              flight per CTA the loads already keep HBM busy, and a
+//              prefetch only queues ahead of them in the same copy engine);
 //   warp 1     MMA issuer (one thread): S_j = Q K_j^T into the TMEM S buffer
 //              (A = Q from TMEM) once tile j has landed and S_{j-1} has been
 //              read; O += P_i V_i (A = P from TMEM, V read from the same smem
@@ -340,21 +341,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             for (int c = 0; c < nq; ++c)
                 tma_load_3d(sQst + c * QCH_BYTES, &tm_q, 64 * (5 * half + c), mt * BM, b,
                             bar(C::B_QFULL));
-            // rows of tile t into L2 ahead of its load; the peer CTA reads other
-            // columns of the same rows, so one of the two prefetches
-            auto prefetch_tile = [&](int t) {
-                if (half == 0 && t < ntiles) {
-                    const int j = k0 + t * BN, n = min(BN, k1 - j);
-                    prefetch_l2(p.gathered + ((size_t)b * p.K + j) * p.row_bytes,
-                                (uint32_t)(n * p.row_bytes));
-                }
-            };
             int issued = 0;
             bool ok = true;
             for (int i = 0; i < ntiles && ok; ++i) {
-                if (i == 0)
-                    for (int t = 2; t < NG + 2; ++t) prefetch_tile(t);
-                if (i >= 2) prefetch_tile(i + NG);
                 if (i == 2) {
                     // tile groups 2-3 hold the staged Q until it has moved to TMEM
                     if (!mbar_wait(bar(C::B_QREADY), 0)) {
