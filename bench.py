@@ -133,12 +133,20 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def algorithmic(w, counts_sum):
-    """Algorithmic bytes / flops of one step (per-unit figures x units)."""
+def algorithmic(w, counts_sum, in_place=False):
+    """Algorithmic bytes / flops of one step (per-unit figures x units).
+
+    Gathered rows: the resolve reads every hit row and writes every row to the
+    gathered buffer (plus the miss rows into their slots); in place it writes
+    only the miss rows into their slots. Either way attention reads each
+    selected row once."""
     B, K, rb = w.B, w.K, w.row_bytes
     rows = B * K
     res, hot, miss = counts_sum
-    resolve_hbm = (res + hot) * rb + rows * rb + miss * rb + rows * 12
+    if in_place:
+        resolve_hbm = miss * rb + rows * 12
+    else:
+        resolve_hbm = (res + hot) * rb + rows * rb + miss * rb + rows * 12
     resolve_link = miss * rb
     q = B * w.T * w.H * 576 * 2
     out = B * w.T * w.H * 512 * 2 + B * w.T * w.H * 4
@@ -208,11 +216,11 @@ def run_gpu(args):
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         if agent:
-            gw = GpuAgent(w, stream=stream)
+            gw = GpuAgent(w, stream=stream, in_place=args.in_place)
             plan = list(W.agent_steps(w))
             lists = [torch.from_numpy(st.topk).to("cuda") for st in plan]
         else:
-            gw = GpuWorkload(w, stream=stream)
+            gw = GpuWorkload(w, stream=stream, in_place=args.in_place)
             plan = None
             lists = [gw.topk[s] for s in range(w.steps)]
         nq = min(len(lists), 16)
@@ -297,7 +305,7 @@ def run_gpu(args):
     rows_per_s = ws * w.B * w.K / (res_ms * 1e-3)
 
     per_step_counts = cnt_sum / steps
-    r_hbm, r_link, d_bytes, flops = algorithmic(w, per_step_counts)
+    r_hbm, r_link, d_bytes, flops = algorithmic(w, per_step_counts, args.in_place)
     hbm_peak, tf_peak, peak_kind = _peaks()
     kernels = {
         "resolve": {"ms": res_ms, "achieved": r_hbm / (res_ms * 1e-3) / 1e9, "unit": "GB/s",
@@ -336,6 +344,8 @@ def run_gpu(args):
         "config": {"workload": desc, "global_batch": w.B * ws, "top_k": w.K,
                    "heads": w.H, "query_tokens": w.T, "ctx": w.ctx,
                    "parallelism": f"replicas x{ws} (requests sharded by rank, no collective)",
+                   "rows": ("read in place from the pool by attention (no gathered buffer)"
+                            if args.in_place else "gathered by the resolve, then read by attention"),
                    "l2": ("flushed before every timed step: 256 MiB written, then 256 MiB of "
                           "other data read (clean, cold L2); the flush is outside the events")},
         "resolved_rows_per_s": round(rows_per_s, 1),
@@ -530,6 +540,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="requests per step (default: the workload's; smaller only for profiling)")
+    ap.add_argument("--in-place", action="store_true",
+                    help="attention reads rows from the pool by id; no gathered buffer")
     ap.add_argument("--ctx", type=int, default=0,
                     help="override the context length (profiling captures only)")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(DESCS),

@@ -15,8 +15,11 @@ import workloads as W
 class GpuWorkload:
     """A workload's pool, its request tables and the step buffers on cuda:0."""
 
-    def __init__(self, w: W.Workload, stream=None, build_topk: bool = True):
+    def __init__(self, w: W.Workload, stream=None, build_topk: bool = True,
+                 in_place: bool = False):
+        """in_place: no gathered buffer; attention reads the rows from the pool."""
         self.w = w
+        self.in_place = in_place
         lay = self.lay = W.layout(w)
         has_host = bool((lay.page_host >= 0).any())
         dtype = hs.HS_BF16 if w.dtype == "bf16" else hs.HS_FP8_E4M3_ROWSCALE
@@ -39,8 +42,12 @@ class GpuWorkload:
         B, K, rb = w.B, w.K, w.row_bytes
         self.req_ids = torch.arange(B, dtype=torch.int32, device=dev)
         self.resolved = torch.empty((B, K), dtype=torch.int32, device=dev)
-        self.gathered = torch.empty((B, K, rb), dtype=torch.uint8, device=dev)
-        self.gscale = torch.empty((B, K), dtype=torch.float32, device=dev) if w.dtype == "fp8" else None
+        if in_place:
+            self.gathered = self.gscale = None
+        else:
+            self.gathered = torch.empty((B, K, rb), dtype=torch.uint8, device=dev)
+            self.gscale = (torch.empty((B, K), dtype=torch.float32, device=dev)
+                           if w.dtype == "fp8" else None)
         self.counts = torch.empty((B, 3), dtype=torch.int32, device=dev)
         self.out = torch.empty((B, w.T, w.H, 512), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((B, w.T, w.H), dtype=torch.float32, device=dev)
@@ -65,8 +72,9 @@ class GpuAgent:
     """The agent mix in a GPU pool: all pages have a GPU block and a host copy;
     each step maps only the pages its residency state keeps resident."""
 
-    def __init__(self, w: "W.AgentMix", stream=None):
+    def __init__(self, w: "W.AgentMix", stream=None, in_place: bool = False):
         self.w = w
+        self.in_place = in_place
         lay = self.lay = W.agent_layout(w)
         self.pool = hs.Pool(dtype=hs.HS_FP8_E4M3_ROWSCALE if w.dtype == "fp8" else hs.HS_BF16,
                             n_gpu_blocks=lay.n_gpu_blocks, n_host_blocks=lay.n_host_blocks,
@@ -92,8 +100,12 @@ class GpuAgent:
         self.req_ids = torch.arange(B, dtype=torch.int32, device=dev)
         self.ctx = torch.empty(B, dtype=torch.int32, device=dev)
         self.resolved = torch.empty((B, K), dtype=torch.int32, device=dev)
-        self.gathered = torch.empty((B, K, rb), dtype=torch.uint8, device=dev)
-        self.gscale = torch.empty((B, K), dtype=torch.float32, device=dev) if w.dtype == "fp8" else None
+        if in_place:
+            self.gathered = self.gscale = None
+        else:
+            self.gathered = torch.empty((B, K, rb), dtype=torch.uint8, device=dev)
+            self.gscale = (torch.empty((B, K), dtype=torch.float32, device=dev)
+                           if w.dtype == "fp8" else None)
         self.counts = torch.empty((B, 3), dtype=torch.int32, device=dev)
         self.out = torch.empty((B, w.T, w.H, 512), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((B, w.T, w.H), dtype=torch.float32, device=dev)

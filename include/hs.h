@@ -146,15 +146,19 @@ hs_status hs_pool_get_error(hs_pool_t pool, uint32_t *device_error_bits);
  *   d_topk_idx  int32 [B][K] token positions, -1 = padding; any order
  *   d_resolved  int32 [B][K] out: pool row id of each entry, -1 if unresolved
  *   d_gathered  [B][K][row_bytes] out: the rows, packed in list order (zeros
- *               for unresolved entries); 16-byte aligned
- *   d_gathered_scale float [B][K] out (FP8 pools; NULL for BF16)
+ *               for unresolved entries); 16-byte aligned. NULL: no gathered
+ *               copy; the rows stay in the pool for hs_sparse_mla_decode to
+ *               read in place (resolved ids only, misses still copied into
+ *               their hot slots)
+ *   d_gathered_scale float [B][K] out (FP8 pools with d_gathered; NULL for
+ *               BF16 pools and whenever d_gathered is NULL)
  *   d_counts    int32 [B][3] out: entries resolved as (resident, hot, miss)
  * Per request, with clock c = previous clock + 1: an entry whose page is
  * resident resolves in place; one held in the hot buffer resolves to its slot
  * and gets stamp c; all hits are stamped before any miss is placed. Misses, in
  * ascending position, take the unprotected slots (stamp < c) with the smallest
  * (stamp, slot) keys; each miss row (and scale) is read from the pinned host
- * arena into its slot and into d_gathered. A repeated missing position is
+ * arena into its slot (and into d_gathered). A repeated missing position is
  * served once (first in list order). Requires 1 <= K <= max_topk. */
 hs_status hs_resolve_topk(hs_pool_t pool, int32_t B, const int32_t *d_req_ids,
                           const int32_t *d_topk_idx, int32_t K, int32_t *d_resolved,
@@ -165,6 +169,9 @@ hs_status hs_resolve_topk(hs_pool_t pool, int32_t B, const int32_t *d_req_ids,
  * selected latent rows (解决 KV 缓存内存压力; 稀疏MLA的核心思想). Query token t of request b sits at position L_b - T + t
  * (L_b = ctx_len of d_req_ids[b]) and attends to entry j iff d_resolved[b][j]
  * >= 0 and d_topk_idx[b][j] <= L_b - T + t.
+ *   d_gathered / d_gathered_scale: as written by hs_resolve_topk; or both
+ *           NULL to read each entry's row (and FP8 scale) in place from the
+ *           pool by its d_resolved id (entries with id -1 read a zero row)
  *   d_q     bf16 [B][T][H][576]
  *   d_out   bf16 [B][T][H][512] = softmax(sm_scale * q.k_j) weighted sum of k_j[0:512]
  *   d_lse   float [B][T][H]      = ln sum_j exp(sm_scale * q.k_j); -inf if none valid

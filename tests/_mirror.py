@@ -51,11 +51,23 @@ def compare_resolve(gw, ot, res_o, gat_o, gsc_o, cnt_o, err_o, err_gpu, step, ro
     sel = slice(None) if rows is None else rows
     assert np.array_equal(res[sel], res_o[sel]), f"resolved differs at step {step}"
     assert np.array_equal(cnt[sel], cnt_o[sel]), f"counts differ at step {step}"
-    gat = gw.gathered.cpu().numpy()
-    assert np.array_equal(gat[sel], gat_o[sel]), f"gathered rows differ at step {step}"
-    if gsc_o is not None:
-        gsc = gw.gscale.cpu().numpy()
-        assert np.array_equal(gsc[sel].view(np.uint32), gsc_o[sel].view(np.uint32))
+    if gw.gathered is not None:
+        gat = gw.gathered.cpu().numpy()
+        assert np.array_equal(gat[sel], gat_o[sel]), f"gathered rows differ at step {step}"
+        if gsc_o is not None:
+            gsc = gw.gscale.cpu().numpy()
+            assert np.array_equal(gsc[sel].view(np.uint32), gsc_o[sel].view(np.uint32))
+    else:
+        # rows stay in the pool: every resolved row id must hold the bytes (and
+        # scale) the oracle gathered for that entry
+        rows = gw.pool.gpu_rows().cpu().numpy()
+        r = res[sel]
+        ok = r >= 0
+        assert np.array_equal(rows[r[ok]], gat_o[sel][ok]), f"pool rows differ at step {step}"
+        assert not gat_o[sel][~ok].any(), "absent entries gather zeros"
+        if gsc_o is not None:
+            sc = gw.pool.gpu_scales().cpu().numpy()
+            assert np.array_equal(sc[r[ok]].view(np.uint32), gsc_o[sel][ok].view(np.uint32))
     assert err_gpu == err_o, f"error bits {err_gpu} vs oracle {err_o} at step {step}"
     st = gpu_state(gw)
     assert np.array_equal(st["clock"], ot.clock)

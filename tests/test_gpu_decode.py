@@ -30,11 +30,11 @@ def _bits(q):
     return q.cpu().view(torch.int16).numpy().view(np.uint16)
 
 
-def _decode_case(w, steps, sample_rows=None, nthreads=8, topk_override=None):
+def _decode_case(w, steps, sample_rows=None, nthreads=8, topk_override=None, in_place=False):
     import oracle
     from harness import GpuWorkload
     from _mirror import attention_errors, oracle_mirror
-    gw = GpuWorkload(w)
+    gw = GpuWorkload(w, in_place=in_place)
     ot = oracle_mirror(gw)
     lists = gw.topk_host if topk_override is None else topk_override
     worst = (0.0, 0.0)
@@ -104,3 +104,47 @@ def test_decode_edge_cases():
     lists[0, 2, :] = -1                            # request 2: the last three positions only;
     lists[0, 2, :3] = [w.ctx - 1, w.ctx - 2, w.ctx - 3]  # token 0 (position L-4) sees none
     _decode_case(w, 1, topk_override=lists)
+
+
+# ---------------------------------------------------------------- rows read in place
+@pytest.mark.parametrize("name", list(SMALL))
+def test_decode_in_place_parity_small(name):
+    """No gathered buffer: attention gathers the rows from the pool by row id."""
+    w, steps = SMALL[name]
+    _decode_case(w, steps, in_place=True)
+
+
+@pytest.mark.parametrize("name", ["resident", "hybrid"])
+def test_decode_in_place_full_size_sampled(name):
+    _decode_case(W.WORKLOADS[name], 1, sample_rows=256, nthreads=16, in_place=True)
+
+
+def test_decode_in_place_edge_cases():
+    w = W.WORKLOADS["tiny"].scaled(B=3, T=4, H=8, steps=1)
+    lists = np.stack(list(W.topk_lists(w)))
+    lists[0, 0, :] = -1
+    lists[0, 1, :] = -1
+    lists[0, 1, 7] = 4000
+    lists[0, 2, :] = -1
+    lists[0, 2, :3] = [w.ctx - 1, w.ctx - 2, w.ctx - 3]
+    _decode_case(w, 1, topk_override=lists, in_place=True)
+
+
+@pytest.mark.parametrize("name", ["resident", "hybrid_ragged", "noresident"])
+def test_decode_in_place_matches_gathered_bitwise(name):
+    """The same rows reach the same tiles either way, so the outputs are identical."""
+    from harness import GpuWorkload
+    w, _ = SMALL[name]
+    ga, gb = GpuWorkload(w), GpuWorkload(w, in_place=True)
+    for s in range(2):
+        q = W.make_q(w, s, device="cuda")
+        for gw in (ga, gb):
+            gw.resolve(s)
+            gw.decode(s, q)
+        torch.cuda.synchronize()
+        assert ga.pool.get_error() == 0 and gb.pool.get_error() == 0
+        assert torch.equal(ga.resolved, gb.resolved)
+        assert torch.equal(ga.out.view(torch.int16), gb.out.view(torch.int16)), f"out differs, step {s}"
+        assert torch.equal(ga.lse.view(torch.int32), gb.lse.view(torch.int32)), f"lse differs, step {s}"
+    ga.pool.close()
+    gb.pool.close()

@@ -21,10 +21,10 @@ def _lib():
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
 
 
-def _run(w, steps=None, nthreads=4, topk_override=None):
+def _run(w, steps=None, nthreads=4, topk_override=None, in_place=False):
     from harness import GpuWorkload
     from _mirror import compare_resolve, oracle_mirror
-    gw = GpuWorkload(w)
+    gw = GpuWorkload(w, in_place=in_place)
     ot = oracle_mirror(gw)
     lists = gw.topk_host if topk_override is None else topk_override
     n = len(lists) if steps is None else min(steps, len(lists))
@@ -55,6 +55,15 @@ SMALL = {
 @pytest.mark.parametrize("name", list(SMALL))
 def test_resolve_parity_small(name):
     tot = _run(SMALL[name])
+    assert tot.sum() > 0
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_resolve_in_place_parity_small(name):
+    """No gathered buffer: the same ids, counts and LRU state, and every
+    resolved pool row holds the bytes the oracle gathered (misses copied from
+    the host arena straight into their hot slots)."""
+    tot = _run(SMALL[name], in_place=True)
     assert tot.sum() > 0
 
 

@@ -117,8 +117,10 @@ struct Cfg {
 
 struct DecParams {
     const int32_t *resolved, *topk, *req_ids, *ctx;
-    const float *gscale;
+    const float *gscale;        // gathered row scales (FP8, gathered rows)
+    const float *pool_scales;   // pool row scales (FP8, rows read in place)
     const uint8_t *gathered;
+    int zero_row;               // pool row of zeros read for absent entries (in place)
     __nv_bfloat16 *out;
     float *lse, *ws_o, *ws_lse;
     uint32_t *err;
@@ -181,6 +183,17 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t a) {
         "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]),           \
         "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])                                           \
         : "memory")
+
+// Four rows (r0..r3) of a 2-D tensor map, each one box wide starting at
+// column x, to consecutive box-sized places at dst.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int x, int r0, int r1,
+                                            int r2, int r3, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+        : "memory");
+}
 
 template <bool FP8>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
@@ -271,7 +284,7 @@ __device__ __forceinline__ uint32_t x_off(int r, int c) {
     return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
-template <bool FP8>
+template <bool FP8, bool INPLACE>
 __global__ void __launch_bounds__(NTHR, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const DecParams p) {
@@ -336,41 +349,67 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        // Lane 0 loads Q and takes each slot; a tile read from the gathered
+        // buffer is one box per chunk (lane 0), a tile read in place from the
+        // pool is 16 four-row gathers per chunk, one per lane 0..15.
         if (lane == 0) {
             mbar_expect_tx(bar(C::B_QFULL), nq * QCH_BYTES);
             for (int c = 0; c < nq; ++c)
                 tma_load_3d(sQst + c * QCH_BYTES, &tm_q, 64 * (5 * half + c), mt * BM, b,
                             bar(C::B_QFULL));
-            int issued = 0;
-            bool ok = true;
-            for (int i = 0; i < ntiles && ok; ++i) {
-                if (i == 2) {
-                    // tile groups 2-3 hold the staged Q until it has moved to TMEM
-                    if (!mbar_wait(bar(C::B_QREADY), 0)) {
-                        ok = false;
-                        break;
-                    }
-                }
-                const int g = i % NG;
+        }
+        constexpr uint32_t ROWB = FP8 ? 64u : 128u;  // smem bytes of one row of one chunk
+        // in place: pool row ids of this lane's four rows, loaded a tile ahead
+        auto row_ids = [&](int i, int (&rid)[4]) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int j = k0 + i * BN + 4 * lane + q;
+                rid[q] = (INPLACE && lane < 16 && i < ntiles && j < k1)
+                             ? p.resolved[(size_t)b * p.K + j] : -1;
+            }
+        };
+        int rid_next[4];
+        row_ids(0, rid_next);
+        int issued = 0;
+        bool ok = true;
+        for (int i = 0; i < ntiles; ++i) {
+            const int g = i % NG;
+            int go = 0;
+            if (lane == 0) {
                 const uint32_t ph = (uint32_t)(i / NG) & 1u;
-                if (!mbar_wait(bar(C::B_GEMPTY + g), ph ^ 1u) || misc[1]) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t done = bar((FP8 ? C::B_GLANDED : C::B_GFULL) + g);
+                // tile groups 2-3 hold the staged Q until it has moved to TMEM
+                go = (i != 2 || mbar_wait(bar(C::B_QREADY), 0)) &&
+                     mbar_wait(bar(C::B_GEMPTY + g), ph ^ 1u) && !misc[1];
+            }
+            if (!__shfl_sync(0xffffffffu, go, 0)) {
+                ok = false;
+                break;
+            }
+            const uint32_t done = bar((FP8 ? C::B_GLANDED : C::B_GFULL) + g);
+            if (INPLACE) {
+                int rid[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) rid[q] = rid_next[q] >= 0 ? rid_next[q] : p.zero_row;
+                row_ids(i + 1, rid_next);
+                if (lane == 0) mbar_expect_tx(done, NLC * (FP8 ? FCH_BYTES : KCH_BYTES));
+                if (lane < 16)
+                    for (int lc = 0; lc < NLC; ++lc)
+                        tma_gather4(slot(g, lc) + (FP8 ? KCH_BYTES - FCH_BYTES : 0) + 4u * ROWB * lane,
+                                    &tm_k, 64 * (4 * half + lc), rid[0], rid[1], rid[2], rid[3], done);
+            } else if (lane == 0) {
                 mbar_expect_tx(done, NLC * (FP8 ? FCH_BYTES : KCH_BYTES));
                 for (int lc = 0; lc < NLC; ++lc)
                     tma_load_3d(slot(g, lc) + (FP8 ? KCH_BYTES - FCH_BYTES : 0), &tm_k,
                                 64 * (4 * half + lc), k0 + i * BN, b, done);
-                ++issued;
             }
-            if (!ok) {
-                fail();
-                // let the copies this thread started land before the CTA exits
-                mbar_wait(bar(C::B_QFULL), 0);
-                for (int i = issued - 1; i >= 0 && i >= issued - NG; --i)
-                    mbar_wait(bar((FP8 ? C::B_GLANDED : C::B_GFULL) + i % NG), (i / NG) & 1);
-            }
+            ++issued;
+        }
+        if (!ok && lane == 0) {
+            fail();
+            // let the copies this warp started land before the CTA exits
+            mbar_wait(bar(C::B_QFULL), 0);
+            for (int i = issued - 1; i >= 0 && i >= issued - NG; --i)
+                mbar_wait(bar((FP8 ? C::B_GLANDED : C::B_GFULL) + i % NG), (i / NG) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -429,7 +468,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const long long first = (long long)((r >= 0 && r < p.max_req) ? p.ctx[r] : 0) - p.T;
         const int32_t *res_b = p.resolved + (size_t)b * p.K;
         const int32_t *top_b = p.topk + (size_t)b * p.K;
-        const float *gs = FP8 ? p.gscale + (size_t)b * p.K : nullptr;
+        const float *gs = (FP8 && !INPLACE) ? p.gscale + (size_t)b * p.K : nullptr;
         bool ok = true;
         for (int i = 0; i < ntiles; ++i) {
             const int g = i % NG;
@@ -446,7 +485,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const bool in = j < k1;
                 res[h] = in ? res_b[j] : -1;
                 top[h] = in ? top_b[j] : 0;
-                sc[h] = (FP8 && j < p.K) ? gs[j] : 0.f;
+                sc[h] = 0.f;
+                if (FP8)
+                    sc[h] = INPLACE ? (res[h] >= 0 ? p.pool_scales[res[h]] : 0.f)
+                                    : (j < p.K ? gs[j] : 0.f);
             }
             if (FP8) {
                 __half2 s2[2];
@@ -861,27 +903,28 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 3-D map [batch][rows][inner] with a (box_inner x box_rows x 1) box.
+// Map [batch][rows][inner] (rank 3) or [rows][inner] (rank 2, batch 1) with a
+// (box_inner x box_rows) box.
 bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, uint64_t inner,
               uint64_t rows, uint64_t batch, uint64_t row_bytes, uint32_t box_inner,
-              uint32_t box_rows, CUtensorMapSwizzle sw) {
+              uint32_t box_rows, CUtensorMapSwizzle sw, uint32_t rank = 3) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {inner, rows, batch};
     cuuint64_t strides[2] = {row_bytes, row_bytes * rows};
     cuuint32_t box[3] = {box_inner, box_rows, 1};
     cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, dt, 3, const_cast<void *>(ptr), dims, strides, box, es,
+    return fn(m, dt, rank, const_cast<void *>(ptr), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool FP8>
+template <bool FP8, bool INPLACE>
 hs_status launch_decode(dim3 grid, cudaStream_t s, const CUtensorMap &tq, const CUtensorMap &tk,
                         const DecParams &p) {
     static bool ready = false;
     if (!ready) {
-        HS_CUDA_TRY(cudaFuncSetAttribute(decode_tc_kernel<FP8>,
+        HS_CUDA_TRY(cudaFuncSetAttribute(decode_tc_kernel<FP8, INPLACE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_ALLOC));
         ready = true;
     }
@@ -897,8 +940,9 @@ hs_status launch_decode(dim3 grid, cudaStream_t s, const CUtensorMap &tq, const 
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<FP8>, tq, tk, p) == cudaSuccess ? HS_OK
-                                                                                   : HS_ERR_CUDA;
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<FP8, INPLACE>, tq, tk, p) == cudaSuccess
+               ? HS_OK
+               : HS_ERR_CUDA;
 }
 
 }  // namespace
@@ -914,13 +958,17 @@ extern "C" hs_status hs_sparse_mla_decode(hs_pool_t pool, int32_t B, int32_t T, 
                                           const int32_t *d_topk_idx, const int32_t *d_req_ids,
                                           float sm_scale, void *d_out, float *d_lse,
                                           void *d_workspace, size_t ws_bytes, void *stream) {
-    if (!pool || !d_q || !d_gathered || !d_resolved || !d_topk_idx || !d_req_ids || !d_out || !d_lse)
+    if (!pool || !d_q || !d_resolved || !d_topk_idx || !d_req_ids || !d_out || !d_lse)
         return HS_ERR_INVALID_ARG;
     if (B < 0 || T < 1 || T > 32767 || H < 1 || K < 1 || B > 65535 ||
         (int64_t)T * H > (int64_t)BM * 65535)
         return HS_ERR_INVALID_ARG;
     const bool fp8 = pool->cfg.dtype == HS_FP8_E4M3_ROWSCALE;
-    if (fp8 != (d_gathered_scale != nullptr)) return HS_ERR_INVALID_ARG;
+    // rows from the gathered buffer (with their scales for FP8), or in place
+    // from the pool by row id (no gathered buffer and no scales)
+    const bool inplace = d_gathered == nullptr;
+    if (inplace ? d_gathered_scale != nullptr : fp8 != (d_gathered_scale != nullptr))
+        return HS_ERR_INVALID_ARG;
     if (((uintptr_t)d_q | (uintptr_t)d_gathered | (uintptr_t)d_out) & 15u) return HS_ERR_INVALID_ARG;
     if (B == 0) return HS_OK;
     const Plan pl = make_plan(B, T, H, K);
@@ -932,11 +980,20 @@ extern "C" hs_status hs_sparse_mla_decode(hs_pool_t pool, int32_t B, int32_t T, 
     if (!make_map(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_q, hs::kDim, pl.M, B, 2 * hs::kDim, 64,
                   BM, CU_TENSOR_MAP_SWIZZLE_128B))
         return HS_ERR_CUDA;
-    const bool ok_k =
-        fp8 ? make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, d_gathered, hs::kDim, K, B, hs::kDim, 64,
-                       BN, CU_TENSOR_MAP_SWIZZLE_NONE)
-            : make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_gathered, hs::kDim, K, B,
-                       2 * hs::kDim, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B);
+    bool ok_k;
+    if (inplace) {
+        // the pool as [rows][576] with one-row boxes, for four-row gathers
+        const uint64_t nrows = (uint64_t)(pool->cfg.n_gpu_blocks + 1) * hs::kPage;
+        ok_k = fp8 ? make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, pool->d_rows, hs::kDim, nrows, 1,
+                              hs::kDim, 64, 1, CU_TENSOR_MAP_SWIZZLE_NONE, 2)
+                   : make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pool->d_rows, hs::kDim, nrows, 1,
+                              2 * hs::kDim, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B, 2);
+    } else {
+        ok_k = fp8 ? make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, d_gathered, hs::kDim, K, B, hs::kDim,
+                              64, BN, CU_TENSOR_MAP_SWIZZLE_NONE)
+                   : make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_gathered, hs::kDim, K, B,
+                              2 * hs::kDim, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B);
+    }
     if (!ok_k) return HS_ERR_CUDA;
 
     DecParams p{};
@@ -945,7 +1002,9 @@ extern "C" hs_status hs_sparse_mla_decode(hs_pool_t pool, int32_t B, int32_t T, 
     p.req_ids = d_req_ids;
     p.ctx = pool->d_ctx;
     p.gscale = d_gathered_scale;
+    p.pool_scales = pool->d_scales;
     p.gathered = static_cast<const uint8_t *>(d_gathered);
+    p.zero_row = (int)(pool->cfg.n_gpu_blocks * hs::kPage);
     p.row_bytes = fp8 ? hs::kDim : 2 * hs::kDim;
     p.out = static_cast<__nv_bfloat16 *>(d_out);
     p.lse = d_lse;
@@ -965,8 +1024,10 @@ extern "C" hs_status hs_sparse_mla_decode(hs_pool_t pool, int32_t B, int32_t T, 
     p.scale_log2 = sm_scale * 1.4426950408889634f;
 
     const dim3 grid(2 * pl.nsplit, pl.mtiles, B);
-    const hs_status st = fp8 ? launch_decode<true>(grid, s, tq, tk, p)
-                             : launch_decode<false>(grid, s, tq, tk, p);
+    const hs_status st = fp8 ? (inplace ? launch_decode<true, true>(grid, s, tq, tk, p)
+                                        : launch_decode<true, false>(grid, s, tq, tk, p))
+                             : (inplace ? launch_decode<false, true>(grid, s, tq, tk, p)
+                                        : launch_decode<false, false>(grid, s, tq, tk, p));
     if (st != HS_OK) return st;
     if (pl.nsplit > 1) {
         const int rows = B * pl.M;

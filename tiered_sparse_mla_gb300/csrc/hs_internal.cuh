@@ -29,6 +29,7 @@ struct DevPool {
     const int32_t *ctx;        // [max_req]
     uint32_t *err;             // device error word
     int max_req, max_pages, max_ctx, C, HB, row_bytes;
+    int zero_row;              // a row of zeros (and scale 0) after the pool's blocks
 };
 
 }  // namespace hs
@@ -68,6 +69,7 @@ struct hs_pool {
         p.C = cfg.hot_rows;
         p.HB = hb;
         p.row_bytes = row_bytes;
+        p.zero_row = (int)(cfg.n_gpu_blocks * hs::kPage);
         return p;
     }
 };

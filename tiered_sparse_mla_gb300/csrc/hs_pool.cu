@@ -120,7 +120,7 @@ hs_status hs_pool_create(const hs_pool_config *cfg_in, void *stream, hs_pool_t *
     if (cfg.max_requests < 1 || cfg.max_ctx < 1 || cfg.n_gpu_blocks < 1 || cfg.n_host_blocks < 0)
         return HS_ERR_INVALID_ARG;
     // row ids are int32 on the device
-    if (cfg.n_gpu_blocks * hs::kPage >= (int64_t(1) << 31) ||
+    if ((cfg.n_gpu_blocks + 1) * hs::kPage >= (int64_t(1) << 31) ||
         cfg.n_host_blocks * hs::kPage >= (int64_t(1) << 31))
         return HS_ERR_INVALID_ARG;
 
@@ -141,7 +141,9 @@ hs_status hs_pool_create(const hs_pool_config *cfg_in, void *stream, hs_pool_t *
     p->hb = cfg.hot_rows / hs::kPage;
     const int64_t R = cfg.max_requests, C = cfg.hot_rows;
     const bool fp8 = cfg.dtype == HS_FP8_E4M3_ROWSCALE;
-    const size_t gpu_rows = (size_t)cfg.n_gpu_blocks * hs::kPage;
+    // one block more than the caller's: a block of zero rows (scale 0) that
+    // attention reads in place of absent entries
+    const size_t gpu_rows = (size_t)(cfg.n_gpu_blocks + 1) * hs::kPage;
     const size_t host_rows = (size_t)cfg.n_host_blocks * hs::kPage;
 
     bool ok = true;
@@ -189,6 +191,13 @@ hs_status hs_pool_create(const hs_pool_config *cfg_in, void *stream, hs_pool_t *
     if (st == HS_OK) st = fill(p->d_clock, R, 0, s);
     if (st == HS_OK) st = fill(p->d_ctx, R, 0, s);
     if (st == HS_OK && cudaMemsetAsync(p->d_err, 0, sizeof(uint32_t), s) != cudaSuccess)
+        st = HS_ERR_CUDA;
+    const size_t zero0 = (size_t)cfg.n_gpu_blocks * hs::kPage;
+    if (st == HS_OK && cudaMemsetAsync(p->d_rows + zero0 * p->row_bytes, 0,
+                                       (size_t)hs::kPage * p->row_bytes, s) != cudaSuccess)
+        st = HS_ERR_CUDA;
+    if (st == HS_OK && fp8 &&
+        cudaMemsetAsync(p->d_scales + zero0, 0, hs::kPage * sizeof(float), s) != cudaSuccess)
         st = HS_ERR_CUDA;
     if (st == HS_OK) st = hs_resolve_prepare(p);
     if (st == HS_OK && cudaStreamSynchronize(s) != cudaSuccess) st = HS_ERR_CUDA;

@@ -107,16 +107,18 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
     const int j0 = (g - 1) * chunk;  // first list entry of a worker
     const int nloc = g == 0 ? 0 : max(0, min(K, j0 + chunk) - j0);
     const size_t row0 = (size_t)bi * K + (g == 0 ? 0 : j0);  // first gathered row of this CTA
-    const bool fp8 = gscale != nullptr;
+    const bool fp8 = P.scales != nullptr;
+    const bool gath = gathered != nullptr;  // else rows are read in place by attention
 
     if (r < 0 || r >= P.max_req) {
         // the whole cluster takes this branch (same request), so no barrier waits
         for (int l = tid; l < nloc; l += NT) {
             resolved[row0 + l] = -1;
-            if (fp8) gscale[row0 + l] = 0.f;
+            if (gath && fp8) gscale[row0 + l] = 0.f;
         }
-        for (int i = tid; i < nloc * V; i += NT)
-            hs::st_v4(gathered + row0 * RB + (size_t)i * 16, make_uint4(0, 0, 0, 0));
+        if (gath)
+            for (int i = tid; i < nloc * V; i += NT)
+                hs::st_v4(gathered + row0 * RB + (size_t)i * 16, make_uint4(0, 0, 0, 0));
         if (g == 0 && tid < 3) counts[bi * 3 + tid] = 0;
         if (g == 0 && tid == 0) atomicOr(P.err, HS_DEVERR_BAD_REQUEST);
         return;
@@ -191,7 +193,7 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
         // ------------------------------------------------------------ phase 2
         // every row whose gathered position is known: pool rows for hits, host
         // rows for misses (placed into their slots after barrier B), zeros
-        {
+        if (gath) {
             const int nunits = nloc * V;
             uint8_t *gdst = gathered + row0 * RB;
             for (int base = tid; base < nunits; base += NT * UNROLL) {
@@ -213,10 +215,19 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
                 for (int u = 0; u < UNROLL; ++u)
                     if (base + u * NT < nunits) hs::st_v4(gdst + (size_t)(base + u * NT) * 16, v[u]);
             }
+        }
+        {
             for (int l = tid; l < nloc; l += NT) {
                 const int kd = s_kind[l];
+                // in place, miss rows are read only after placement: start
+                // pulling them over the host link into L2 now
+                if (!gath && kd == KIND_MISS)
+                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                                     P.host_rows + (size_t)s_hrow[l] * RB),
+                                 "r"((uint32_t)RB)
+                                 : "memory");
                 if (kd != KIND_MISS) resolved[row0 + l] = kd == KIND_NONE ? -1 : s_src[l];
-                if (fp8) {
+                if (gath && fp8) {
                     float sc = 0.f;
                     if (kd == KIND_RES || kd == KIND_HOT) sc = P.scales[s_src[l]];
                     else if (kd == KIND_MISS) sc = P.host_scales[s_hrow[l]];
@@ -229,12 +240,13 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
         hs::cluster_wait();    // barrier B: rank 0 has placed every miss
 
         // ------------------------------------------------------------ phase 3
-        // placed miss rows: gathered -> hot slot; rejected ones: zeroed
+        // placed miss rows: gathered -> hot slot (in place: host -> hot slot);
+        // rejected ones: zeroed in the gathered buffer
         {
             __syncthreads();  // this CTA's gathered writes are visible to all its threads
             const int nm = s_misc[0];
             const int nunits = nm * V;
-            uint8_t *gsrc = gathered + row0 * RB;
+            uint8_t *gsrc = gath ? gathered + row0 * RB : nullptr;
             for (int base = tid; base < nunits; base += NT * UNROLL) {
                 uint4 v[UNROLL];
                 int dst[UNROLL], l_[UNROLL], part_[UNROLL];
@@ -248,14 +260,16 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
                         l_[u] = l;
                         part_[u] = part;
                         dst[u] = s_src[l];
-                        if (dst[u] >= 0) v[u] = hs::ld_v4(gsrc + (size_t)l * RB + part * 16);
+                        if (dst[u] >= 0)
+                            v[u] = gath ? hs::ld_v4(gsrc + (size_t)l * RB + part * 16)
+                                        : hs::ld_v4(P.host_rows + (size_t)s_hrow[l] * RB + part * 16);
                     }
                 }
 #pragma unroll
                 for (int u = 0; u < UNROLL; ++u) {
                     if (dst[u] >= 0)
                         hs::st_v4(P.rows + (size_t)dst[u] * RB + part_[u] * 16, v[u]);
-                    else if (dst[u] == -1)
+                    else if (dst[u] == -1 && gath)
                         hs::st_v4(gsrc + (size_t)l_[u] * RB + part_[u] * 16, make_uint4(0, 0, 0, 0));
                 }
             }
@@ -264,8 +278,13 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
                 const int d = s_src[l];
                 resolved[row0 + l] = d;
                 if (fp8) {
-                    if (d >= 0) P.scales[d] = gscale[row0 + l];
-                    else gscale[row0 + l] = 0.f;
+                    if (!gath) {
+                        if (d >= 0) P.scales[d] = P.host_scales[s_hrow[l]];
+                    } else if (d >= 0) {
+                        P.scales[d] = gscale[row0 + l];
+                    } else {
+                        gscale[row0 + l] = 0.f;
+                    }
                 }
             }
         }
@@ -487,12 +506,14 @@ extern "C" hs_status hs_resolve_topk(hs_pool_t pool, int32_t B, const int32_t *d
                                      const int32_t *d_topk_idx, int32_t K, int32_t *d_resolved,
                                      void *d_gathered, float *d_gathered_scale, int32_t *d_counts,
                                      void *stream) {
-    if (!pool || B < 0 || !d_req_ids || !d_topk_idx || !d_resolved || !d_gathered || !d_counts)
+    if (!pool || B < 0 || !d_req_ids || !d_topk_idx || !d_resolved || !d_counts)
         return HS_ERR_INVALID_ARG;
     if (K < 1 || K > pool->cfg.max_topk || K > pool->cfg.hot_rows) return HS_ERR_CAPACITY;
     if (B > 65535) return HS_ERR_INVALID_ARG;
     const bool fp8 = pool->cfg.dtype == HS_FP8_E4M3_ROWSCALE;
-    if (fp8 != (d_gathered_scale != nullptr)) return HS_ERR_INVALID_ARG;
+    // gathered rows (and, for FP8 pools, their scales) or neither
+    if (d_gathered ? fp8 != (d_gathered_scale != nullptr) : d_gathered_scale != nullptr)
+        return HS_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(d_gathered) & 15u) != 0) return HS_ERR_INVALID_ARG;
     if (B == 0) return HS_OK;
     return hs_launch_resolve(pool, B, d_req_ids, d_topk_idx, K, d_resolved, d_gathered,
