@@ -184,6 +184,16 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t a) {
         "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])                                           \
         : "memory")
 
+// A box of a 4-D tensor map (coordinates innermost first).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int c0, int c1, int c2, int c3,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
 // Four rows (r0..r3) of a 2-D tensor map, each one box wide starting at
 // column x, to consecutive box-sized places at dst.
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int x, int r0, int r1,
@@ -308,6 +318,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const uint32_t sXin = base + C::OFF_XIN, sXout = base + C::OFF_XOUT;
     auto bar = [&](int i) { return base + C::OFF_BAR + 8u * (uint32_t)i; };
     auto slot = [&](int g, int lc) { return sR + (uint32_t)((g * NLC + lc) * KCH_BYTES); };
+    // FP8: the e4m3 codes of chunk lc, packed in the upper half of the tile group
+    auto codes = [&](int g, int lc) {
+        return sR + (uint32_t)(g * NLC * KCH_BYTES + NLC * FCH_BYTES + lc * FCH_BYTES);
+    };
     auto fail = [&]() {
         misc[1] = 1;
         atomicOr(p.err, HS_DEVERR_TIMEOUT);
@@ -394,13 +408,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (lane == 0) mbar_expect_tx(done, NLC * (FP8 ? FCH_BYTES : KCH_BYTES));
                 if (lane < 16)
                     for (int lc = 0; lc < NLC; ++lc)
-                        tma_gather4(slot(g, lc) + (FP8 ? KCH_BYTES - FCH_BYTES : 0) + 4u * ROWB * lane,
+                        tma_gather4((FP8 ? codes(g, lc) : slot(g, lc)) + 4u * ROWB * lane,
                                     &tm_k, 64 * (4 * half + lc), rid[0], rid[1], rid[2], rid[3], done);
             } else if (lane == 0) {
+                // all five chunks of the tile's 64 rows in one box: [chunk][row][64]
                 mbar_expect_tx(done, NLC * (FP8 ? FCH_BYTES : KCH_BYTES));
-                for (int lc = 0; lc < NLC; ++lc)
-                    tma_load_3d(slot(g, lc) + (FP8 ? KCH_BYTES - FCH_BYTES : 0), &tm_k,
-                                64 * (4 * half + lc), k0 + i * BN, b, done);
+                tma_load_4d(FP8 ? codes(g, 0) : slot(g, 0), &tm_k, 0, k0 + i * BN, 4 * half, b, done);
             }
             ++issued;
         }
@@ -495,8 +508,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
                 for (int h = 0; h < 2; ++h) s2[h] = __float2half2_rn(sc[h]);
                 for (int lc = 0; lc < NLC; ++lc) {
-                    // the e4m3 codes sit in the upper half of the slot; every row
-                    // is read before any f16 row (which may overlap them) is written
+                    // The codes of all five chunks sit packed in the upper half of
+                    // the group. Chunk lc's f16 rows overlap only the codes of
+                    // chunks <= lc, so in ascending order with all of a chunk's
+                    // codes read before any of its f16 rows is written, nothing
+                    // is overwritten before it has been read.
                     const uint32_t sl = slot(g, lc);
                     uint4 raw4[2][4];
                     if (ok) {
@@ -504,8 +520,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         for (int h = 0; h < 2; ++h)
 #pragma unroll
                             for (int q = 0; q < 4; ++q)
-                                raw4[h][q] = ld_shared_v4(sl + (KCH_BYTES - FCH_BYTES) +
-                                                          (lane + 32 * h) * 64 + 16 * q);
+                                raw4[h][q] = ld_shared_v4(codes(g, lc) + (lane + 32 * h) * 64 + 16 * q);
                     }
                     __syncwarp();
                     if (!ok) continue;
@@ -919,6 +934,21 @@ bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, uint64_t 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Rows of 9 chunks of 64 elements, as a 4-D map (element, row, chunk,
+// request) with a (64 x BN x NLC x 1) box.
+bool make_chunk_map(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, uint64_t rows,
+                    uint64_t batch, uint64_t row_bytes, uint64_t chunk_bytes, CUtensorMapSwizzle sw) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {64, rows, 9, batch};
+    cuuint64_t strides[3] = {row_bytes, chunk_bytes, row_bytes * rows};
+    cuuint32_t box[4] = {64, (cuuint32_t)BN, (cuuint32_t)NLC, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return fn(m, dt, 4, const_cast<void *>(ptr), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <bool FP8, bool INPLACE>
 hs_status launch_decode(dim3 grid, cudaStream_t s, const CUtensorMap &tq, const CUtensorMap &tk,
                         const DecParams &p) {
@@ -989,10 +1019,12 @@ extern "C" hs_status hs_sparse_mla_decode(hs_pool_t pool, int32_t B, int32_t T, 
                    : make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pool->d_rows, hs::kDim, nrows, 1,
                               2 * hs::kDim, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B, 2);
     } else {
-        ok_k = fp8 ? make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, d_gathered, hs::kDim, K, B, hs::kDim,
-                              64, BN, CU_TENSOR_MAP_SWIZZLE_NONE)
-                   : make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_gathered, hs::kDim, K, B,
-                              2 * hs::kDim, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B);
+        // [B][K][9 chunks][64] viewed as (column, row, chunk, request) so that one
+        // box brings all five chunks of 64 rows, chunk-major in shared memory
+        ok_k = fp8 ? make_chunk_map(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, d_gathered, K, B, hs::kDim, 64,
+                                    CU_TENSOR_MAP_SWIZZLE_NONE)
+                   : make_chunk_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_gathered, K, B,
+                                    2 * hs::kDim, 128, CU_TENSOR_MAP_SWIZZLE_128B);
     }
     if (!ok_k) return HS_ERR_CUDA;
 
