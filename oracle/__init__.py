@@ -151,9 +151,14 @@ class OracleTiers:
         self.pos_to_slot[r] = -1
         self.clock[r] = 0
 
-    def resolve(self, req_ids, topk, formulation: int = 0, nthreads: int = 1):
+    def resolve(self, req_ids, topk, formulation: int = 0, nthreads: int = 1,
+                union: bool = False):
         """One decode step. Returns (resolved [B][K] int32, gathered [B][K][rb] uint8,
-        gathered_scale [B][K] f32 or None, counts [B][3] int32, error bits)."""
+        gathered_scale [B][K] f32 or None, counts [B][3] int32, error bits).
+
+        union: each list is the union of several lists sharing the request's hot
+        state (per-token MTP lists, concatenated); a missing position repeated
+        in it is served once and all its occurrences resolve to that row."""
         req_ids = _c(req_ids, np.int32)
         topk = _c(topk, np.int32)
         B, K = topk.shape
@@ -162,7 +167,8 @@ class OracleTiers:
         gscale = np.empty((B, K), np.float32) if self.fp8 else None
         counts = np.empty((B, 3), np.int32)
         st = self._state()
-        err = lib().or_resolve(C.byref(st), B, _p(req_ids), _p(topk), K, formulation,
+        err = lib().or_resolve(C.byref(st), B, _p(req_ids), _p(topk), K,
+                               formulation | (2 if union else 0),
                                _p(resolved), _p(gathered), _p(gscale), _p(counts), nthreads)
         return resolved, gathered, gscale, counts, int(err)
 

@@ -120,9 +120,14 @@ static int64_t or_hot_row(const or_state *S, int32_t r, int32_t slot)
     return (int64_t)blk * OR_PAGE + slot % OR_PAGE;
 }
 
-/* Resolve one request's list. formulation 0: each miss scans for the argmin
- * (stamp, slot) unprotected slot; formulation 1: the unprotected keys are
- * sorted once and the i-th miss takes the i-th key. */
+/* Resolve one request's list. Bit 0 of `formulation` picks the LRU rule's
+ * form: 0, each miss scans for the argmin (stamp, slot) unprotected slot; 1,
+ * the unprotected keys are sorted once and the i-th miss takes the i-th key.
+ * Bit 1 set: the list is the union of several lists sharing one hot state
+ * (the MTP draft tokens' own lists, [A] 与 vLLM 栈的集成, speculative
+ * decoding), so a missing position repeated in it is served once and every
+ * occurrence resolves to that row (or is rejected with it); without bit 1 the
+ * repeats are rejected as errors. */
 static uint32_t or_resolve_one(const or_state *S, int32_t r, const int32_t *topk, int32_t K,
                                int formulation, int32_t *resolved, uint8_t *gathered,
                                float *gathered_scale, int32_t *counts)
@@ -175,17 +180,24 @@ static uint32_t or_resolve_one(const or_state *S, int32_t r, const int32_t *topk
     qsort(miss, n_miss, sizeof(or_miss), or_cmp_miss);
     or_key *keys = NULL;
     int32_t n_keys = 0, next_key = 0;
-    if (formulation == 1) {
+    if (formulation & 1) {
         keys = malloc(sizeof(or_key) * C);
         for (int32_t s = 0; s < C; ++s)
             if (stamp[s] < c) { keys[n_keys].stamp = stamp[s]; keys[n_keys].slot = s; n_keys++; }
         qsort(keys, n_keys, sizeof(or_key), or_cmp_key);
     }
+    const int uni = (formulation & 2) != 0;
+    int32_t last_row = -1; /* row the previous distinct missing position got (-1 = rejected) */
     for (int32_t i = 0; i < n_miss; ++i) {
         int32_t p = miss[i].p, j = miss[i].j;
-        if (i > 0 && miss[i - 1].p == p) { err |= OR_ERR_DUPLICATE; continue; }
+        if (i > 0 && miss[i - 1].p == p) {
+            if (!uni) { err |= OR_ERR_DUPLICATE; continue; }
+            if (last_row >= 0) { resolved[j] = last_row; counts[2]++; }
+            continue;
+        }
+        last_row = -1;
         int32_t v = -1;
-        if (formulation == 0) {
+        if ((formulation & 1) == 0) {
             for (int32_t s = 0; s < C; ++s) {
                 if (stamp[s] >= c) continue;
                 if (v < 0 || stamp[s] < stamp[v]) v = s; /* ties keep the lower slot */
@@ -204,6 +216,7 @@ static uint32_t or_resolve_one(const or_state *S, int32_t r, const int32_t *topk
         memcpy(S->pool_rows + drow * rb, S->host_rows + hrow * rb, rb);
         if (S->pool_scales) S->pool_scales[drow] = S->host_scales[hrow];
         resolved[j] = (int32_t)drow;
+        last_row = (int32_t)drow;
         counts[2]++;
     }
     free(keys);

@@ -257,3 +257,51 @@ def test_invariants_on_workloads(oracle_lib, name, kw):
         assert total[0] > 0 and total[1] > 0 and total[2] > 0
     else:
         assert total[1] > 0 and total[2] > 0
+
+
+# ---------------------------------------------------------------- union of lists
+@pytest.mark.parametrize("seed", range(30))
+def test_union_reduces_to_deduplicated_resolve(oracle_lib, seed):
+    """Union mode (per-token MTP lists sharing one hot state): resolving a list
+    with repeated positions equals resolving it with every repeat blanked (the
+    pinned single-list rule), then giving each repeat its first occurrence's
+    row. The hot state ends identical, and no repeat error is raised."""
+    rng = np.random.default_rng(2000 + seed)
+    n_pages, ctx, C, K, page_gpu, page_host = _random_case(rng)
+    hot_block = n_pages
+    mk = lambda: _tiers(oracle_lib, page_gpu[None], page_host[None], np.array([[hot_block]]),
+                        ctx, C, 16, 64 * (n_pages + 1), 64 * n_pages,
+                        np.random.default_rng(seed), max_ctx=64 * n_pages)
+    u, d = mk(), mk()
+    universe = rng.choice(64 * n_pages + 8, size=min(64 * n_pages, 3 * C), replace=False) - 4
+    for step in range(12):
+        # a few lists over a small working set, concatenated: repeats are common
+        topk = rng.choice(universe, size=K, replace=True).astype(np.int32)
+        topk[rng.random(K) < 0.1] = -1
+        first = {}
+        rep = np.zeros(K, bool)
+        for j, p in enumerate(topk.tolist()):
+            if p == -1:
+                continue
+            if p in first:
+                rep[j] = True
+            else:
+                first[p] = j
+        blank = topk.copy()
+        blank[rep] = -1
+        ru, gu, _, cu, eu = u.resolve([0], topk[None], union=True)
+        rd, gd, _, cd, ed = d.resolve([0], blank[None])
+        want = rd[0].copy()
+        for j in np.nonzero(rep)[0]:
+            want[j] = rd[0][first[int(topk[j])]]
+        assert np.array_equal(ru[0], want)
+        assert eu == ed and not (eu & 2)
+        assert cu.sum() == cd.sum() + int((want[rep] >= 0).sum())
+        for a, b in ((u.tag, d.tag), (u.stamp, d.stamp), (u.pos_to_slot, d.pos_to_slot),
+                     (u.clock, d.clock), (u.pool_rows, d.pool_rows)):
+            assert np.array_equal(a, b)
+        # every occurrence of a position names one row, and its bytes are gathered
+        for j in range(K):
+            if ru[0, j] >= 0:
+                assert ru[0, j] == ru[0, first[int(topk[j])]]
+                assert np.array_equal(gu[0, j], u.pool_rows[ru[0, j]])
