@@ -133,24 +133,32 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def algorithmic(w, counts_sum, in_place=False):
+def algorithmic(w, counts_sum, in_place=False, per_token=None):
     """Algorithmic bytes / flops of one step (per-unit figures x units).
 
     Gathered rows: the resolve reads every hit row and writes every row to the
     gathered buffer (plus the miss rows into their slots); in place it writes
     only the miss rows into their slots. Either way attention reads each
-    selected row once."""
+    selected row once.
+
+    per_token = (distinct rows, distinct misses) per step when every query
+    token has its own list: entries = B*T*K; a row that several tokens select
+    is read from HBM (and a missing one from the host) once."""
     B, K, rb = w.B, w.K, w.row_bytes
-    rows = B * K
     res, hot, miss = counts_sum
-    if in_place:
-        resolve_hbm = miss * rb + rows * 12
+    if per_token is None:
+        rows = entries = B * K
     else:
-        resolve_hbm = (res + hot) * rb + rows * rb + miss * rb + rows * 12
+        entries = B * w.T * K
+        rows, miss = per_token
+    if in_place:
+        resolve_hbm = miss * rb + entries * 12
+    else:
+        resolve_hbm = (res + hot) * rb + entries * rb + miss * rb + entries * 12
     resolve_link = miss * rb
     q = B * w.T * w.H * 576 * 2
     out = B * w.T * w.H * 512 * 2 + B * w.T * w.H * 4
-    decode_bytes = rows * rb + q + out + rows * 8
+    decode_bytes = rows * rb + q + out + entries * 8
     flops = 2.0 * B * w.T * w.H * K * (576 + 512)
     return resolve_hbm, resolve_link, decode_bytes, flops
 
@@ -213,6 +221,9 @@ def run_gpu(args):
         # shrinks the pool, for profiler captures; not a bench line
         w = w.scaled(ctx=args.ctx)
     steps = args.steps or DEFAULT_STEPS[name]
+    per_token = bool(args.per_token)
+    if per_token and (agent or w.T < 2):
+        raise SystemExit("--per-token needs a workload with several query tokens (hybrid)")
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         if agent:
@@ -220,9 +231,14 @@ def run_gpu(args):
             plan = list(W.agent_steps(w))
             lists = [torch.from_numpy(st.topk).to("cuda") for st in plan]
         else:
-            gw = GpuWorkload(w, stream=stream, in_place=args.in_place)
+            gw = GpuWorkload(w, stream=stream, in_place=args.in_place, per_token=per_token)
             plan = None
             lists = [gw.topk[s] for s in range(w.steps)]
+            if per_token:
+                # distinct selected positions of each step (the rows attention
+                # must read at least once)
+                uniq = [sum(len(np.unique(gw.topk_host[s][b][gw.topk_host[s][b] >= 0]))
+                            for b in range(w.B)) for s in range(w.steps)]
         nq = min(len(lists), 16)
         qs = [W.make_q(w, s, device="cuda") for s in range(nq)]
         flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
@@ -254,11 +270,21 @@ def run_gpu(args):
         q = qs[s % nq]
         if ev is not None:
             ev[0].record(stream)
-        gw.pool.resolve_topk(gw.req_ids, t, gw.resolved, gw.gathered, gw.gscale, gw.counts, stream)
+        if per_token:
+            gw.pool.resolve_topk_union(gw.req_ids, t, gw.resolved, gw.gathered, gw.gscale,
+                                       gw.counts, stream)
+        else:
+            gw.pool.resolve_topk(gw.req_ids, t, gw.resolved, gw.gathered, gw.gscale, gw.counts,
+                                 stream)
         if ev is not None:
             ev[1].record(stream)
-        gw.pool.sparse_mla_decode(q, gw.gathered, gw.gscale, gw.resolved, t, gw.req_ids,
-                                  w.sm_scale, gw.out, gw.lse, gw.workspace, stream)
+        if per_token:
+            gw.pool.sparse_mla_decode_per_token(q, gw.gathered, gw.gscale, gw.resolved, t,
+                                                gw.req_ids, w.sm_scale, gw.out, gw.lse,
+                                                gw.workspace, stream)
+        else:
+            gw.pool.sparse_mla_decode(q, gw.gathered, gw.gscale, gw.resolved, t, gw.req_ids,
+                                      w.sm_scale, gw.out, gw.lse, gw.workspace, stream)
         if ev is not None:
             ev[2].record(stream)
 
@@ -276,6 +302,10 @@ def run_gpu(args):
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     counts_acc = torch.zeros(3, dtype=torch.int64, device="cuda")
+    # distinct placed misses: each takes one slot and retags it (outside the events)
+    slot_tag = gw.pool.tables()["slot_tag"]
+    tag_prev = torch.empty_like(slot_tag)
+    retagged = torch.zeros((), dtype=torch.int64, device="cuda")
     if ws > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -286,9 +316,13 @@ def run_gpu(args):
         for s in range(steps):
             if s > 0:
                 prepare(s)
+            if per_token:
+                tag_prev.copy_(slot_tag)
             l2_flush()
             step(s, evs[s])
             counts_acc += gw.counts.sum(0)
+            if per_token:
+                retagged += (slot_tag != tag_prev).sum()
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
     wall = time.perf_counter() - t0
@@ -305,7 +339,12 @@ def run_gpu(args):
     rows_per_s = ws * w.B * w.K / (res_ms * 1e-3)
 
     per_step_counts = cnt_sum / steps
-    r_hbm, r_link, d_bytes, flops = algorithmic(w, per_step_counts, args.in_place)
+    pt = None
+    if per_token:
+        pt = (sum(uniq[s % n_lists] for s in range(steps)) / steps,
+              float(retagged.item()) / steps)
+        rows_per_s = ws * w.B * w.T * w.K / (res_ms * 1e-3)
+    r_hbm, r_link, d_bytes, flops = algorithmic(w, per_step_counts, args.in_place, pt)
     hbm_peak, tf_peak, peak_kind = _peaks()
     kernels = {
         "resolve": {"ms": res_ms, "achieved": r_hbm / (res_ms * 1e-3) / 1e9, "unit": "GB/s",
@@ -331,10 +370,14 @@ def run_gpu(args):
                 "frac": round(kt["achieved"] / kt["peak"], 4), "traffic": kt["traffic"],
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"}
 
-    launches = 2 + (1 if hs.hs_decode_workspace_bytes(w.B, w.T, w.H, w.K) > 0 else 0)
+    launches = 2 + (1 if (hs.hs_decode_workspace_bytes(w.B * w.T, 1, w.H, w.K) if per_token else
+                          hs.hs_decode_workspace_bytes(w.B, w.T, w.H, w.K)) > 0 else 0)
     desc = DESCS[name] if (agent or w.B == W.WORKLOADS[name].B) else f"{DESCS[name]} [batch {w.B}]"
     if not agent and w.ctx != W.WORKLOADS[name].ctx:
         desc += f" [context {w.ctx}]"
+    if per_token:
+        desc += (f" [one top-{w.K} list per query token (10% fresh per later token), the "
+                 f"{w.T} lists of a request resolved as one union]")
     line = {
         "metric": METRIC, "value": round(steps_per_s, 2), "unit": "decode steps/s",
         "n_gpus": ws, "steps": steps, "warmup": args.warmup,
@@ -352,6 +395,8 @@ def run_gpu(args):
         "resolve_ms": round(res_ms, 5), "decode_ms": round(dec_ms, 5),
         "counts_per_step": {"resident": float(per_step_counts[0]), "hot": float(per_step_counts[1]),
                             "miss": float(per_step_counts[2])},
+        **({"per_token": {"entries_per_step": w.B * w.T * w.K, "distinct_rows_per_step": pt[0],
+                          "distinct_misses_per_step": pt[1]}} if per_token else {}),
         "roofline": roofline,
         "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
                     for k, v in kernels.items()},
@@ -540,6 +585,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="requests per step (default: the workload's; smaller only for profiling)")
+    ap.add_argument("--per-token", action="store_true",
+                    help="one top-K list per query token: union resolve + per-token decode")
     ap.add_argument("--in-place", action="store_true",
                     help="attention reads rows from the pool by id; no gathered buffer")
     ap.add_argument("--ctx", type=int, default=0,

@@ -16,16 +16,21 @@ class GpuWorkload:
     """A workload's pool, its request tables and the step buffers on cuda:0."""
 
     def __init__(self, w: W.Workload, stream=None, build_topk: bool = True,
-                 in_place: bool = False):
-        """in_place: no gathered buffer; attention reads the rows from the pool."""
+                 in_place: bool = False, per_token: bool = False):
+        """in_place: no gathered buffer; attention reads the rows from the pool.
+        per_token: one top-K list per query token (topk [steps][B][T][K]); the
+        resolve takes each request's T lists as one union, the decode gives
+        each token its own list."""
         self.w = w
         self.in_place = in_place
+        self.per_token = per_token
+        KL = w.T * w.K if per_token else w.K  # entries resolved per request
         lay = self.lay = W.layout(w)
         has_host = bool((lay.page_host >= 0).any())
         dtype = hs.HS_BF16 if w.dtype == "bf16" else hs.HS_FP8_E4M3_ROWSCALE
         self.pool = hs.Pool(dtype=dtype, n_gpu_blocks=lay.n_gpu_blocks,
                             n_host_blocks=lay.n_host_blocks if has_host else 0,
-                            max_requests=w.B, max_ctx=w.ctx, max_topk=w.K,
+                            max_requests=w.B, max_ctx=w.ctx, max_topk=KL,
                             hot_rows=w.hot_rows, stream=stream)
         for r in range(w.B):
             self.pool.request_init(r, w.ctx)
@@ -39,33 +44,48 @@ class GpuWorkload:
                         W.row_seed(w, "host"), gen_device="cuda")
         torch.cuda.synchronize()
         dev = "cuda"
-        B, K, rb = w.B, w.K, w.row_bytes
+        B, rb = w.B, w.row_bytes
         self.req_ids = torch.arange(B, dtype=torch.int32, device=dev)
-        self.resolved = torch.empty((B, K), dtype=torch.int32, device=dev)
+        self.resolved = torch.empty((B, KL), dtype=torch.int32, device=dev)
         if in_place:
             self.gathered = self.gscale = None
         else:
-            self.gathered = torch.empty((B, K, rb), dtype=torch.uint8, device=dev)
-            self.gscale = (torch.empty((B, K), dtype=torch.float32, device=dev)
+            self.gathered = torch.empty((B, KL, rb), dtype=torch.uint8, device=dev)
+            self.gscale = (torch.empty((B, KL), dtype=torch.float32, device=dev)
                            if w.dtype == "fp8" else None)
         self.counts = torch.empty((B, 3), dtype=torch.int32, device=dev)
         self.out = torch.empty((B, w.T, w.H, 512), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((B, w.T, w.H), dtype=torch.float32, device=dev)
-        ws = hs.hs_decode_workspace_bytes(B, w.T, w.H, K)
+        ws = (hs.hs_decode_workspace_bytes(B * w.T, 1, w.H, w.K) if per_token
+              else hs.hs_decode_workspace_bytes(B, w.T, w.H, w.K))
         self.workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
-        self.topk_host = np.stack(list(W.topk_lists(w))) if build_topk else None
+        self.topk_host = None
+        if build_topk:
+            lists = list(W.topk_lists(w))
+            if per_token:
+                lists = [W.token_lists(w, b, s) for s, b in enumerate(lists)]
+            self.topk_host = np.stack(lists)
         self.topk = torch.from_numpy(self.topk_host).to(dev) if build_topk else None
 
     def resolve(self, step: int, topk=None, stream=None):
         t = self.topk[step] if topk is None else topk
-        self.pool.resolve_topk(self.req_ids, t, self.resolved, self.gathered, self.gscale,
-                               self.counts, stream)
+        if self.per_token:
+            self.pool.resolve_topk_union(self.req_ids, t, self.resolved, self.gathered,
+                                         self.gscale, self.counts, stream)
+        else:
+            self.pool.resolve_topk(self.req_ids, t, self.resolved, self.gathered, self.gscale,
+                                   self.counts, stream)
 
     def decode(self, step: int, q, topk=None, stream=None):
         t = self.topk[step] if topk is None else topk
-        self.pool.sparse_mla_decode(q, self.gathered, self.gscale, self.resolved, t,
-                                    self.req_ids, self.w.sm_scale, self.out, self.lse,
-                                    self.workspace, stream)
+        if self.per_token:
+            self.pool.sparse_mla_decode_per_token(q, self.gathered, self.gscale, self.resolved,
+                                                  t, self.req_ids, self.w.sm_scale, self.out,
+                                                  self.lse, self.workspace, stream)
+        else:
+            self.pool.sparse_mla_decode(q, self.gathered, self.gscale, self.resolved, t,
+                                        self.req_ids, self.w.sm_scale, self.out, self.lse,
+                                        self.workspace, stream)
 
 
 class GpuAgent:

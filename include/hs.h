@@ -68,7 +68,8 @@ typedef struct {
     int32_t max_ctx;       /* largest context length of any request (tokens)       */
     int32_t hot_rows;      /* hot-buffer rows per request; multiple of page_size;
                               0 selects 2*max_topk                                  */
-    int32_t max_topk;      /* largest K; must not exceed hot_rows                   */
+    int32_t max_topk;      /* largest K (1 .. 8192) of any resolve: one list of at
+                              most hot_rows entries, or a union of several lists  */
 } hs_pool_config;
 
 /* Device pointers to the pool's tables, for inspection after synchronising the
@@ -159,11 +160,27 @@ hs_status hs_pool_get_error(hs_pool_t pool, uint32_t *device_error_bits);
  * ascending position, take the unprotected slots (stamp < c) with the smallest
  * (stamp, slot) keys; each miss row (and scale) is read from the pinned host
  * arena into its slot (and into d_gathered). A repeated missing position is
- * served once (first in list order). Requires 1 <= K <= max_topk. */
+ * served once (first in list order). Requires 1 <= K <= min(max_topk, hot_rows). */
 hs_status hs_resolve_topk(hs_pool_t pool, int32_t B, const int32_t *d_req_ids,
                           const int32_t *d_topk_idx, int32_t K, int32_t *d_resolved,
                           void *d_gathered, float *d_gathered_scale, int32_t *d_counts,
                           void *stream);
+
+/* hs_resolve_topk for several top-K lists per request resolved against the
+ * request's one hot state (推测性解码: each step's resolve plan is shared by the
+ * request's speculative tokens). d_topk_idx [B][K] holds, per request, the
+ * concatenation of its tokens' lists (K = tokens x per-token top-K; each token's
+ * list holds distinct positions, lists may overlap). Results, layouts and
+ * errors are those of hs_resolve_topk except for repeated positions: every
+ * occurrence of a position resolves to the same row and counts in d_counts;
+ * for a missing position the first occurrence in list order takes the LRU
+ * slot and copies the row, the later ones share it (or are all rejected with
+ * it). No HS_DEVERR_DUPLICATE is raised. Requires 1 <= K <= max_topk; distinct
+ * missing positions beyond the free slots are rejected (HS_DEVERR_CAPACITY). */
+hs_status hs_resolve_topk_union(hs_pool_t pool, int32_t B, const int32_t *d_req_ids,
+                                const int32_t *d_topk_idx, int32_t K, int32_t *d_resolved,
+                                void *d_gathered, float *d_gathered_scale, int32_t *d_counts,
+                                void *stream);
 
 /* Sparse MLA decode over the gathered rows: attention restricted to the K
  * selected latent rows (解决 KV 缓存内存压力; 稀疏MLA的核心思想). Query token t of request b sits at position L_b - T + t
@@ -186,6 +203,22 @@ hs_status hs_sparse_mla_decode(hs_pool_t pool, int32_t B, int32_t T, int32_t H, 
                                float sm_scale, void *d_out, float *d_lse, void *d_workspace,
                                size_t ws_bytes, void *stream);
 size_t hs_decode_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t K);
+
+/* hs_sparse_mla_decode with one top-K list per query token (the lists that
+ * hs_resolve_topk_union resolved). List (b, t) of K entries is row b*T + t of
+ * d_resolved / d_topk_idx ([B][T][K]) and of d_gathered ([B][T][K][row_bytes],
+ * scales [B][T][K]) or, with both NULL, read in place from the pool. Query
+ * token t of request b sits at position L_b - T + t and attends to entry j of
+ * its own list iff d_resolved[b][t][j] >= 0 and d_topk_idx[b][t][j] <= L_b - T + t.
+ * q, out and lse are laid out as in hs_sparse_mla_decode. The workspace needs
+ * hs_decode_workspace_bytes(B * T, 1, H, K) bytes. Requires B * T <= 65535,
+ * H <= 128*65535; other requirements as hs_sparse_mla_decode. */
+hs_status hs_sparse_mla_decode_per_token(hs_pool_t pool, int32_t B, int32_t T, int32_t H,
+                                         int32_t K, const void *d_q, const void *d_gathered,
+                                         const float *d_gathered_scale, const int32_t *d_resolved,
+                                         const int32_t *d_topk_idx, const int32_t *d_req_ids,
+                                         float sm_scale, void *d_out, float *d_lse,
+                                         void *d_workspace, size_t ws_bytes, void *stream);
 
 /* hs_sparse_mla_decode without a caller-provided workspace. This entry point
  * has no counterpart in the pages; it exists for callers that cannot allocate

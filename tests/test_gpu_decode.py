@@ -148,3 +148,83 @@ def test_decode_in_place_matches_gathered_bitwise(name):
         assert torch.equal(ga.lse.view(torch.int32), gb.lse.view(torch.int32)), f"lse differs, step {s}"
     ga.pool.close()
     gb.pool.close()
+
+
+# ---------------------------------------------------------------- one list per query token
+def _per_token_case(w, steps, sample_rows=None, nthreads=8, in_place=False, lists=None):
+    """Union resolve + per-token decode on the GPU; on the oracle side the union
+    resolve, then each (request, token) attends over its own list as a
+    one-token batch entry whose context ends at its position L - T + t."""
+    import oracle
+    from harness import GpuWorkload
+    from _mirror import attention_errors, oracle_mirror
+    gw = GpuWorkload(w, in_place=in_place, per_token=True, build_topk=lists is None)
+    ot = oracle_mirror(gw)
+    lists = gw.topk_host if lists is None else lists
+    B, T, H, K = w.B, w.T, w.H, w.K
+    L1 = (w.ctx - T + 1 + np.tile(np.arange(T), B)).astype(np.int32)  # per list (b, t)
+    for s in range(steps):
+        t = torch.from_numpy(np.ascontiguousarray(lists[s])).cuda()
+        q = W.make_q(w, s, device="cuda")
+        gw.resolve(s, topk=t)
+        gw.decode(s, q, topk=t)
+        torch.cuda.synchronize()
+        assert gw.pool.get_error() == 0
+        flat = np.ascontiguousarray(lists[s].reshape(B, T * K))
+        res, gat, gsc, _, err = ot.resolve(np.arange(B), flat, nthreads=nthreads, union=True)
+        assert err == 0
+        sel = None
+        if sample_rows is not None:
+            rng = np.random.default_rng(200 + s)
+            n = B * T * H
+            idx = np.sort(rng.choice(n, size=min(sample_rows, n), replace=False))
+            sel = np.stack([idx // H, np.zeros_like(idx), idx % H], 1).astype(np.int32)
+        o_ref, l_ref = oracle.sparse_mla_decode(
+            _bits(q).reshape(B * T, 1, H, -1), gat.reshape(B * T, K, -1),
+            None if gsc is None else gsc.reshape(B * T, K), res.reshape(B * T, K),
+            lists[s].reshape(B * T, K), L1, w.sm_scale, sel=sel, nthreads=nthreads)
+        out, lse = gw.out, gw.lse
+        if sel is not None:
+            bt = sel[:, 0]
+            out = gw.out[bt // T, bt % T, sel[:, 2]]
+            lse = gw.lse[bt // T, bt % T, sel[:, 2]]
+        rel, dl = attention_errors(out, lse, o_ref, l_ref)
+        assert rel.max() <= TOL[w.dtype], f"step {s}: max rel err {rel.max():.3e}"
+        assert dl.size == 0 or dl.max() <= LSE_TOL, f"step {s}: max lse err {dl.max():.3e}"
+    gw.pool.close()
+
+
+PER_TOKEN = {
+    "hybrid_mtp": (W.WORKLOADS["hybrid"].scaled(B=2, ctx=32768, resident_tail=4096, H=32,
+                                                 steps=3), 3),
+    "hybrid_ragged": (W.WORKLOADS["hybrid"].scaled(B=2, ctx=16384, resident_tail=2048, K=1000,
+                                                    hot_rows=2048, tail=100, H=24, T=3,
+                                                    steps=2), 2),
+    "resident_bf16": (W.WORKLOADS["resident"].scaled(B=2, ctx=16384, H=64, T=2, steps=2), 2),
+}
+
+
+@pytest.mark.parametrize("name", list(PER_TOKEN))
+@pytest.mark.parametrize("in_place", [False, True])
+def test_decode_per_token_parity_small(name, in_place):
+    w, steps = PER_TOKEN[name]
+    _per_token_case(w, steps, in_place=in_place)
+
+
+@pytest.mark.parametrize("in_place", [False, True])
+def test_decode_per_token_full_size_sampled(in_place):
+    """16 requests x 1M context, 4 tokens with their own top-2048 lists, 128 heads."""
+    _per_token_case(W.WORKLOADS["hybrid"], 1, sample_rows=256, nthreads=16, in_place=in_place)
+
+
+def test_decode_per_token_edge_cases():
+    """A token whose own list is empty, one with a single entry, and lists
+    holding positions after a token's own position (masked for it only)."""
+    w = W.WORKLOADS["tiny"].scaled(B=2, T=4, H=8, steps=1)
+    base = next(iter(W.topk_lists(w)))
+    lists = W.token_lists(w, base, 0)[None].copy()
+    lists[0, 0, 1, :] = -1                         # request 0, token 1: nothing
+    lists[0, 0, 2, :] = -1
+    lists[0, 0, 2, 5] = 1000                       # token 2: one entry
+    lists[0, 1, 0, :3] = [w.ctx - 1, w.ctx - 2, w.ctx - 3]  # after token 0 (L - 4): masked
+    _per_token_case(w, 1, lists=lists)

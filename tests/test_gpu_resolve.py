@@ -49,6 +49,9 @@ SMALL = {
     "noresident": W.WORKLOADS["noresident"].scaled(B=4, ctx=65536, steps=5),
     "noresident_small_k": W.WORKLOADS["noresident"].scaled(B=5, ctx=4096, K=37, hot_rows=128,
                                                             steps=7),
+    # more miss rows per CTA than its shared memory stages: the rest are read
+    # from the host directly
+    "noresident_bf16": W.WORKLOADS["noresident"].scaled(B=2, ctx=32768, dtype="bf16", steps=3),
 }
 
 
@@ -72,6 +75,67 @@ def test_resolve_parity_full_size(name, steps):
     """The full-size workloads, first steps, every request compared."""
     tot = _run(W.WORKLOADS[name], steps=steps, nthreads=16)
     assert tot.sum() == W.WORKLOADS[name].B * W.WORKLOADS[name].K * steps
+
+
+def _run_union(w, steps, in_place=False, nthreads=8, lists=None):
+    """Per-token lists resolved as one union per request, against the oracle's
+    union resolve of the same concatenated lists."""
+    from harness import GpuWorkload
+    from _mirror import compare_resolve, oracle_mirror
+    gw = GpuWorkload(w, in_place=in_place, per_token=True, build_topk=lists is None)
+    ot = oracle_mirror(gw)
+    lists = gw.topk_host if lists is None else lists
+    tot = np.zeros(3, np.int64)
+    for s in range(steps):
+        flat = np.ascontiguousarray(lists[s].reshape(w.B, -1))
+        gw.resolve(s, topk=torch.from_numpy(flat).cuda())
+        err = gw.pool.get_error()
+        out = ot.resolve(np.arange(w.B), flat, nthreads=nthreads, union=True)
+        compare_resolve(gw, ot, *out, err, s)
+        tot += out[3].sum(axis=0)
+    gw.pool.close()
+    return tot
+
+
+UNION = {
+    "hybrid_mtp": W.WORKLOADS["hybrid"].scaled(B=3, ctx=65536, resident_tail=8192, steps=5),
+    "hybrid_ragged": W.WORKLOADS["hybrid"].scaled(B=2, ctx=32768, resident_tail=4096, K=1000,
+                                                   hot_rows=2048, tail=100, T=3, steps=4),
+    "noresident_mtp": W.WORKLOADS["noresident"].scaled(B=3, ctx=65536, T=4, steps=4),
+    "resident_mtp": W.WORKLOADS["resident"].scaled(B=2, ctx=16384, T=2, steps=3),
+}
+
+
+@pytest.mark.parametrize("name", list(UNION))
+@pytest.mark.parametrize("in_place", [False, True])
+def test_resolve_union_parity(name, in_place):
+    """Per-token lists: every occurrence of a repeated position resolves to the
+    same row, only the first takes an LRU slot; ids, counts, bytes and state
+    bit-exact."""
+    w = UNION[name]
+    tot = _run_union(w, w.steps, in_place=in_place)
+    assert tot.sum() > 0
+
+
+def test_resolve_union_capacity_and_repeats():
+    """A union whose distinct misses exceed the free slots: the same rejected
+    entries (all occurrences of a rejected position) and error bits as the
+    oracle; positions repeated inside one token's list are served once too."""
+    w = W.WORKLOADS["noresident"].scaled(B=2, ctx=16384, K=200, hot_rows=256, T=3, steps=2)
+    base = list(W.topk_lists(w))
+    lists = np.stack([W.token_lists(w, b, s, fresh=0.5) for s, b in enumerate(base)])
+    lists[0, 1, 2, :4] = [11, 11, 11, -1]   # repeats within one token's list, padding
+    tot = _run_union(w, 2, lists=lists)
+    assert tot.sum() > 0
+
+
+@pytest.mark.parametrize("in_place", [False, True])
+def test_resolve_union_full_size(in_place):
+    """The MTP workload (16 requests x 1M context, 4 tokens x top-2048 lists,
+    4096-row hot buffers), first steps, every request compared."""
+    w = W.WORKLOADS["hybrid"]
+    tot = _run_union(w, 2, in_place=in_place, nthreads=16)
+    assert tot.sum() == w.B * w.T * w.K * 2
 
 
 def test_resolve_error_paths():

@@ -155,3 +155,28 @@ def test_selected_rows_match_full(oracle_lib):
     idx = [(b * T + t) * H + h for b, t, h in sel]
     np.testing.assert_array_equal(part[0], full[0][idx])
     np.testing.assert_array_equal(part[1], full[1][idx])
+
+
+def test_per_token_layout_equals_shared_list_decode():
+    """One list per query token, each attended as a one-token entry whose
+    context ends at its position L - T + t, equals the T-token decode when
+    every token has the same list (the causal rule of the shared-list form)."""
+    import oracle
+    rng = np.random.default_rng(9)
+    B, T, H, K, L = 2, 4, 3, 40, 300
+    q = rng.integers(0, 1 << 16, size=(B, T, H, 576), dtype=np.uint16)
+    q = (q & 0x3FFF).astype(np.uint16)  # finite, moderate bf16 values
+    rows = rng.standard_normal((B, K, 576)).astype(np.float32)
+    gat = rows.view(np.uint32).astype(np.uint64)
+    gat = ((gat + 0x7FFF + ((gat >> 16) & 1)) >> 16).astype(np.uint16).view(np.uint8)
+    gat = gat.reshape(B, K, 1152)
+    topk = np.stack([rng.choice(L, size=K, replace=False) for _ in range(B)]).astype(np.int32)
+    topk[:, :3] = [L - 1, L - 2, L - 4]       # positions some tokens cannot see
+    res = np.arange(B * K, dtype=np.int32).reshape(B, K)
+    res[:, 5] = -1
+    o1, l1 = oracle.sparse_mla_decode(q, gat, None, res, topk, np.full(B, L, np.int32), 0.05)
+    rep = lambda a: np.repeat(a, T, axis=0)
+    L1 = (L - T + 1 + np.tile(np.arange(T), B)).astype(np.int32)
+    o2, l2 = oracle.sparse_mla_decode(q.reshape(B * T, 1, H, 576), rep(gat), None, rep(res),
+                                      rep(topk), L1, 0.05)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)

@@ -305,3 +305,52 @@ def test_union_reduces_to_deduplicated_resolve(oracle_lib, seed):
             if ru[0, j] >= 0:
                 assert ru[0, j] == ru[0, first[int(topk[j])]]
                 assert np.array_equal(gu[0, j], u.pool_rows[ru[0, j]])
+
+
+def test_token_lists_properties():
+    """Per-token lists: token 0 keeps the step's list, later tokens replace
+    about 10% of it, every list holds distinct positions up to its token's own."""
+    w = W.WORKLOADS["hybrid"].scaled(B=3, ctx=32768, resident_tail=4096, steps=2)
+    for s, base in enumerate(W.topk_lists(w)):
+        tl = W.token_lists(w, base, s)
+        assert tl.shape == (w.B, w.T, w.K) and tl.dtype == np.int32
+        assert np.array_equal(tl[:, 0], base)
+        for b in range(w.B):
+            for t in range(w.T):
+                assert len(np.unique(tl[b, t])) == w.K
+                assert tl[b, t].min() >= 0 and tl[b, t].max() < w.ctx
+                if t:
+                    assert (tl[b, t] != base[b]).sum() == round(0.1 * w.K)
+        assert np.array_equal(tl, W.token_lists(w, base, s))  # seeded
+
+
+def test_union_of_token_lists_on_workload(oracle_lib):
+    """The union resolve of an MTP step's per-token lists: every entry resolves
+    (the distinct positions fit the hot buffer), every occurrence of a position
+    names one row, and the hot buffer holds each distinct missing position once."""
+    import torch
+    w = W.WORKLOADS["hybrid"].scaled(B=2, ctx=16384, resident_tail=2048, hot_rows=512, K=128,
+                                     steps=4, tail=16)
+    lay = W.layout(w)
+    pool = torch.zeros((lay.n_gpu_blocks * PAGE, w.row_bytes), dtype=torch.uint8)
+    host = torch.zeros((lay.n_host_blocks * PAGE, w.row_bytes), dtype=torch.uint8)
+    ps, hs = torch.zeros(pool.shape[0]), torch.zeros(host.shape[0])
+    W.fill_rows(w.dtype, pool, ps, W.row_seed(w, "gpu"))
+    W.fill_rows(w.dtype, host, hs, W.row_seed(w, "host"))
+    ot = oracle_lib.OracleTiers(
+        page_gpu=lay.page_gpu, page_host=lay.page_host, hot_blocks=lay.hot_blocks,
+        ctx_len=np.full(w.B, w.ctx, np.int32), pool_rows=pool.numpy().copy(),
+        pool_scales=ps.numpy().copy(), host_rows=host.numpy(), host_scales=hs.numpy(),
+        hot_rows=w.hot_rows, max_ctx=w.ctx)
+    for s, base in enumerate(W.topk_lists(w)):
+        flat = W.token_lists(w, base, s).reshape(w.B, -1)
+        res, gat, gsc, cnt, err = ot.resolve(np.arange(w.B), flat, union=True)
+        assert err == 0 and (cnt.sum(axis=1) == w.T * w.K).all()
+        for b in range(w.B):
+            row_of = {}
+            for p, r in zip(flat[b].tolist(), res[b].tolist()):
+                assert r >= 0 and row_of.setdefault(p, r) == r
+            tags = ot.tag[b][ot.tag[b] >= 0]
+            assert len(np.unique(tags)) == len(tags)
+            assert np.array_equal(gat[b], ot.pool_rows[res[b]])
+            assert np.array_equal(gsc[b].view(np.uint32), ot.pool_scales[res[b]].view(np.uint32))

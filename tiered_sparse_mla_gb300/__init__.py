@@ -32,7 +32,7 @@ EXPORTED = [
     "hs_gpu_scales", "hs_host_scales", "hs_pool_snapshot", "hs_pool_restore",
     "hs_pool_get_error", "hs_resolve_topk", "hs_sparse_mla_decode",
     "hs_decode_workspace_bytes", "hs_status_string", "hs_sparse_mla_decode_static_ws",
-    "hs_pool_check_bounded_wait",
+    "hs_pool_check_bounded_wait", "hs_resolve_topk_union", "hs_sparse_mla_decode_per_token",
 ]
 HS_STATIC_DECODE_WS_BYTES = 24 << 20
 
@@ -95,6 +95,9 @@ def load() -> C.CDLL:
         "hs_sparse_mla_decode_static_ws": ([vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp,
                                             C.c_float, vp, vp, vp], i32),
         "hs_status_string": ([i32], C.c_char_p),
+        "hs_resolve_topk_union": ([vp, i32, vp, vp, i32, vp, vp, vp, vp, vp], i32),
+        "hs_sparse_mla_decode_per_token": ([vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp,
+                                            C.c_float, vp, vp, vp, sz, vp], i32),
         "hs_pool_check_bounded_wait": ([vp, C.c_uint32, vp], i32),
     }
     for name, (args, res) in sig.items():
@@ -165,6 +168,18 @@ def hs_resolve_topk(pool: int, req_ids, topk_idx, resolved, gathered, gathered_s
         _ptr(gathered_scale), _ptr(counts), _stream(stream)))
 
 
+def hs_resolve_topk_union(pool: int, req_ids, topk_idx, resolved, gathered, gathered_scale,
+                          counts, stream=None):
+    """Resolve of several lists per request as their union (see hs.h). topk_idx
+    int32 [B][T*K] (or [B][T][K]): each request's tokens' lists, concatenated;
+    other tensors as hs_resolve_topk with K replaced by T*K."""
+    B = topk_idx.shape[0]
+    K = topk_idx.numel() // max(B, 1)
+    _check("hs_resolve_topk_union", load().hs_resolve_topk_union(
+        pool, B, _ptr(req_ids), _ptr(topk_idx), K, _ptr(resolved), _ptr(gathered),
+        _ptr(gathered_scale), _ptr(counts), _stream(stream)))
+
+
 def hs_decode_workspace_bytes(B: int, T: int, H: int, K: int) -> int:
     return load().hs_decode_workspace_bytes(B, T, H, K)
 
@@ -177,6 +192,21 @@ def hs_sparse_mla_decode(pool: int, q, gathered, gathered_scale, resolved, topk_
     K = topk_idx.shape[1]
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("hs_sparse_mla_decode", load().hs_sparse_mla_decode(
+        pool, B, T, H, K, _ptr(q), _ptr(gathered), _ptr(gathered_scale), _ptr(resolved),
+        _ptr(topk_idx), _ptr(req_ids), float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+        ws, _stream(stream)))
+
+
+def hs_sparse_mla_decode_per_token(pool: int, q, gathered, gathered_scale, resolved, topk_idx,
+                                   req_ids, sm_scale: float, out, lse, workspace=None,
+                                   stream=None):
+    """Decode with one list per query token (see hs.h). q bf16 [B][T][H][576];
+    topk_idx / resolved int32 [B][T][K]; gathered [B][T][K][row_bytes] or None;
+    workspace of hs_decode_workspace_bytes(B*T, 1, H, K) bytes."""
+    B, T, H, _ = q.shape
+    K = topk_idx.shape[-1]
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("hs_sparse_mla_decode_per_token", load().hs_sparse_mla_decode_per_token(
         pool, B, T, H, K, _ptr(q), _ptr(gathered), _ptr(gathered_scale), _ptr(resolved),
         _ptr(topk_idx), _ptr(req_ids), float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace),
         ws, _stream(stream)))
@@ -322,3 +352,13 @@ class Pool:
                           sm_scale, out, lse, workspace=None, stream=None):
         hs_sparse_mla_decode(self.handle, q, gathered, gathered_scale, resolved, topk_idx,
                              req_ids, sm_scale, out, lse, workspace, stream)
+
+    def resolve_topk_union(self, req_ids, topk_idx, resolved, gathered, gathered_scale, counts,
+                           stream=None):
+        hs_resolve_topk_union(self.handle, req_ids, topk_idx, resolved, gathered,
+                              gathered_scale, counts, stream)
+
+    def sparse_mla_decode_per_token(self, q, gathered, gathered_scale, resolved, topk_idx,
+                                    req_ids, sm_scale, out, lse, workspace=None, stream=None):
+        hs_sparse_mla_decode_per_token(self.handle, q, gathered, gathered_scale, resolved,
+                                       topk_idx, req_ids, sm_scale, out, lse, workspace, stream)

@@ -125,6 +125,7 @@ struct DecParams {
     float *lse, *ws_o, *ws_lse;
     uint32_t *err;
     int B, T, H, K, M, nsplit, kps, max_req, row_bytes;
+    int tpl;  // lists per request: list b is token b % tpl of request b / tpl
     float scale_log2;
 };
 
@@ -477,8 +478,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // Key j of a tile is seen by query token t iff its position is at most
         // L - T + t: store d = clamp(position - (L - T), 0, T), and d = T (seen
         // by none) for unresolved or absent entries; row t then masks d > t.
-        const int r = p.req_ids[b];
-        const long long first = (long long)((r >= 0 && r < p.max_req) ? p.ctx[r] : 0) - p.T;
+        // With one list per token (tpl > 1, T = 1) list b serves token b % tpl
+        // of the request's tpl tokens, whose position is L - tpl + b % tpl.
+        const int r = p.req_ids[b / p.tpl];
+        const long long first = (long long)((r >= 0 && r < p.max_req) ? p.ctx[r] : 0) - p.T -
+                                (p.tpl - 1 - b % p.tpl);
         const int32_t *res_b = p.resolved + (size_t)b * p.K;
         const int32_t *top_b = p.topk + (size_t)b * p.K;
         const float *gs = (FP8 && !INPLACE) ? p.gscale + (size_t)b * p.K : nullptr;
@@ -982,12 +986,14 @@ extern "C" size_t hs_decode_workspace_bytes(int32_t B, int32_t T, int32_t H, int
     return make_plan(B, T, H, K).ws_bytes;
 }
 
-extern "C" hs_status hs_sparse_mla_decode(hs_pool_t pool, int32_t B, int32_t T, int32_t H, int32_t K,
-                                          const void *d_q, const void *d_gathered,
-                                          const float *d_gathered_scale, const int32_t *d_resolved,
-                                          const int32_t *d_topk_idx, const int32_t *d_req_ids,
-                                          float sm_scale, void *d_out, float *d_lse,
-                                          void *d_workspace, size_t ws_bytes, void *stream) {
+namespace {
+// B lists of T query tokens each; tpl > 1 (with T = 1): B / tpl requests whose
+// tpl tokens each have their own list.
+hs_status decode_entry(hs_pool_t pool, int32_t B, int32_t T, int32_t tpl, int32_t H, int32_t K,
+                       const void *d_q, const void *d_gathered, const float *d_gathered_scale,
+                       const int32_t *d_resolved, const int32_t *d_topk_idx,
+                       const int32_t *d_req_ids, float sm_scale, void *d_out, float *d_lse,
+                       void *d_workspace, size_t ws_bytes, void *stream) {
     if (!pool || !d_q || !d_resolved || !d_topk_idx || !d_req_ids || !d_out || !d_lse)
         return HS_ERR_INVALID_ARG;
     if (B < 0 || T < 1 || T > 32767 || H < 1 || K < 1 || B > 65535 ||
@@ -1053,6 +1059,7 @@ extern "C" hs_status hs_sparse_mla_decode(hs_pool_t pool, int32_t B, int32_t T, 
     p.nsplit = pl.nsplit;
     p.kps = pl.kps;
     p.max_req = pool->cfg.max_requests;
+    p.tpl = tpl;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
 
     const dim3 grid(2 * pl.nsplit, pl.mtiles, B);
@@ -1067,6 +1074,30 @@ extern "C" hs_status hs_sparse_mla_decode(hs_pool_t pool, int32_t B, int32_t T, 
         if (cudaGetLastError() != cudaSuccess) return HS_ERR_CUDA;
     }
     return HS_OK;
+}
+}  // namespace
+
+extern "C" hs_status hs_sparse_mla_decode(hs_pool_t pool, int32_t B, int32_t T, int32_t H, int32_t K,
+                                          const void *d_q, const void *d_gathered,
+                                          const float *d_gathered_scale, const int32_t *d_resolved,
+                                          const int32_t *d_topk_idx, const int32_t *d_req_ids,
+                                          float sm_scale, void *d_out, float *d_lse,
+                                          void *d_workspace, size_t ws_bytes, void *stream) {
+    return decode_entry(pool, B, T, 1, H, K, d_q, d_gathered, d_gathered_scale, d_resolved,
+                        d_topk_idx, d_req_ids, sm_scale, d_out, d_lse, d_workspace, ws_bytes,
+                        stream);
+}
+
+extern "C" hs_status hs_sparse_mla_decode_per_token(
+    hs_pool_t pool, int32_t B, int32_t T, int32_t H, int32_t K, const void *d_q,
+    const void *d_gathered, const float *d_gathered_scale, const int32_t *d_resolved,
+    const int32_t *d_topk_idx, const int32_t *d_req_ids, float sm_scale, void *d_out, float *d_lse,
+    void *d_workspace, size_t ws_bytes, void *stream) {
+    if (B < 0 || T < 1 || (int64_t)B * T > 65535) return HS_ERR_INVALID_ARG;
+    // request b's T lists are lists b*T .. b*T+T-1 of one query token each
+    return decode_entry(pool, B * T, 1, T, H, K, d_q, d_gathered, d_gathered_scale, d_resolved,
+                        d_topk_idx, d_req_ids, sm_scale, d_out, d_lse, d_workspace, ws_bytes,
+                        stream);
 }
 
 // ---------------------------------------------------------------- no-allocation variant

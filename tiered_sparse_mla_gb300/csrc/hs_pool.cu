@@ -116,7 +116,6 @@ hs_status hs_pool_create(const hs_pool_config *cfg_in, void *stream, hs_pool_t *
     if (cfg.hot_rows == 0) cfg.hot_rows = 2 * cfg.max_topk;
     if (cfg.hot_rows < 0 || cfg.hot_rows % hs::kPage != 0 || cfg.hot_rows > 16384)
         return HS_ERR_INVALID_ARG;
-    if (cfg.max_topk > cfg.hot_rows) return HS_ERR_CAPACITY;
     if (cfg.max_requests < 1 || cfg.max_ctx < 1 || cfg.n_gpu_blocks < 1 || cfg.n_host_blocks < 0)
         return HS_ERR_INVALID_ARG;
     // row ids are int32 on the device

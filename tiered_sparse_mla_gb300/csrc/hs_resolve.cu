@@ -13,7 +13,10 @@
 // before any miss is placed; misses in ascending position take the unprotected
 // slots (stamp < clock) with the smallest (stamp, slot) keys; residency is
 // checked before the hot buffer; a missing position repeated in one list is
-// served once (first in list order).
+// served once (first in list order). When a request's list is the union of its
+// speculative tokens' lists (推测性解码 shares the request's hot state), every
+// repeat of a missing position resolves to the row its first occurrence took;
+// only the first occurrence updates the LRU state and copies the row.
 //
 // Design (GB300): one thread-block cluster of G CTAs per request. Rank 0 keeps
 // the request's LRU bookkeeping; ranks 1..G-1 ("workers") own K/(G-1) list
@@ -35,6 +38,7 @@
 //   phase 3  workers copy each placed miss row from the gathered buffer into
 //            its hot slot (HBM to HBM) and zero rejected ones.
 // Barriers are hardware cluster barriers: no spin loops.
+#include <algorithm>
 #include <cstdint>
 
 #include "hs_internal.cuh"
@@ -43,6 +47,7 @@ namespace {
 
 constexpr int NT = 512;       // threads per CTA
 constexpr int UNROLL = 4;     // 16-byte vectors in flight per thread and round
+constexpr int UNROLL_H = 8;   // the same for loops that read rows over the host link
 constexpr int KIND_NONE = 0, KIND_RES = 1, KIND_HOT = 2, KIND_MISS = 3;
 
 // Dynamic shared memory layout (bytes), identical in every CTA.
@@ -53,15 +58,19 @@ struct Smem {
     __host__ __device__ size_t off_hrow() const { return off_src() + 4 * (size_t)chunk; }
     __host__ __device__ size_t off_kind() const { return off_hrow() + 4 * (size_t)chunk; }
     __host__ __device__ size_t off_mj() const { return off_kind() + 4 * (size_t)chunk; }
+    // claim: for a miss, the request-level list index of the occurrence that
+    // reads its row from the host (itself, unless a union repeats the position)
+    __host__ __device__ size_t off_claim() const { return off_mj() + 4 * (size_t)chunk; }
     // misc: [0] local misses, [1..3] worker totals, [20..52) warp scan scratch,
     //       [64 + 4g + 0..2] {misses, resident, hot} of worker g (rank 0 only)
-    __host__ __device__ size_t off_misc() const { return off_mj() + 4 * (size_t)chunk; }
+    __host__ __device__ size_t off_misc() const { return off_claim() + 4 * (size_t)chunk; }
     // rank-0 part
     __host__ __device__ size_t off_kin() const { return (off_misc() + 4 * 128 + 15) & ~size_t(15); }
     __host__ __device__ size_t off_keys() const { return off_kin() + 8 * (size_t)W * chunk; }
     __host__ __device__ size_t off_rank() const { return off_keys() + 8 * (size_t)kpad; }
     __host__ __device__ size_t off_victim() const { return off_rank() + 4 * (size_t)K; }
-    __host__ __device__ size_t off_lru() const { return off_victim() + 4 * (size_t)K; }
+    // victims: one per distinct miss, at most one per slot
+    __host__ __device__ size_t off_lru() const { return off_victim() + 4 * (size_t)(K < C ? K : C); }
     __host__ __device__ size_t off_prot() const { return off_lru() + 4 * (size_t)C; }
     __host__ __device__ size_t total() const { return off_prot() + (size_t)C; }
 };
@@ -76,12 +85,40 @@ __device__ __forceinline__ void dsmem_st64(uint32_t a, unsigned long long v) {
     asm volatile("st.shared::cluster.u64 [%0], %1;\n" ::"r"(a), "l"(v) : "memory");
 }
 
+__device__ __forceinline__ void st_shared_v4(void *p, uint4 v) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(const void *p) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(a)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t dyn_smem_bytes() {
+    uint32_t n;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(n));
+    return n;
+}
+
+// Dynamic shared memory of a launch: the layout; with rows kept in the pool,
+// grown (while two CTAs still fit on an SM) so that a worker can stage every
+// row of its share of the list.
+constexpr size_t kStageSmemCap = 110 * 1024;
+
 template <int RB>
 __global__ void __launch_bounds__(NT, 2)
 resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
                const int32_t *__restrict__ topk, int K, int chunk, int G,
                int32_t *__restrict__ resolved, uint8_t *__restrict__ gathered,
-               float *__restrict__ gscale, int32_t *__restrict__ counts) {
+               float *__restrict__ gscale, int32_t *__restrict__ counts, int uni) {
     constexpr int V = RB / 16;  // 16-byte vectors per row
     extern __shared__ __align__(16) unsigned char smem[];
     const int W = G - 1;
@@ -90,6 +127,7 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
     int32_t *s_hrow = reinterpret_cast<int32_t *>(smem + L.off_hrow());
     int32_t *s_kind = reinterpret_cast<int32_t *>(smem + L.off_kind());
     int32_t *s_mj = reinterpret_cast<int32_t *>(smem + L.off_mj());
+    int32_t *s_claim = reinterpret_cast<int32_t *>(smem + L.off_claim());
     int32_t *s_misc = reinterpret_cast<int32_t *>(smem + L.off_misc());
     int32_t *s_warp = s_misc + 20;
     int32_t *s_wcnt = s_misc + 64;  // [G][4], filled by the workers (rank 0 only)
@@ -99,6 +137,10 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
     int32_t *s_victim = reinterpret_cast<int32_t *>(smem + L.off_victim());
     int32_t *s_lru = reinterpret_cast<int32_t *>(smem + L.off_lru());
     uint8_t *s_prot = smem + L.off_prot();
+    // workers: the rank-0 part of their own shared memory stages the miss rows
+    // they read from the host (rows beyond its capacity are read directly)
+    uint8_t *s_stage = smem + L.off_kin();
+    const int ncap = static_cast<int>((dyn_smem_bytes() - L.off_kin()) / RB);
 
     const int tid = threadIdx.x;
     const int g = static_cast<int>(hs::cluster_ctarank());
@@ -134,7 +176,7 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
     int32_t *lru = P.lru + (size_t)r * C;
     int32_t *p2s = P.p2s + (size_t)r * P.max_ctx;
 
-    if (tid == 0) s_misc[0] = s_misc[1] = s_misc[2] = 0;
+    if (tid == 0) s_misc[0] = s_misc[1] = s_misc[2] = s_misc[3] = 0;
     // every CTA of the cluster is running (and has set up its shared memory)
     // before any distributed-shared-memory store below
     __syncthreads();
@@ -170,6 +212,23 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
                     } else {
                         kind = KIND_MISS;
                         hrow = e.y * hs::kPage + (p & 63);
+                        int cj = j0 + l;
+                        if (uni) {
+                            // a union repeats positions across its lists: the
+                            // first occurrence to mark pos_to_slot (-2 - its
+                            // index) reads the row from the host, the others
+                            // take its bytes (rank 0 replaces the mark)
+                            const int old = atomicCAS(&p2s[p], -1, -2 - cj);
+                            if (old <= -2) cj = -2 - old;
+                        }
+                        s_claim[l] = cj;
+                        if (!gath && cj == j0 + l) {
+                            // rows stay in the pool: this occurrence reads the
+                            // row and keeps it in shared memory until its slot
+                            // is known, if there is room (kind bits 4.. = stage + 1)
+                            const int st = atomicAdd(&s_misc[3], 1);
+                            if (st < ncap) kind |= (st + 1) << 4;
+                        }
                         const int m = atomicAdd(&s_misc[0], 1);
                         s_mj[m] = l;
                         dsmem_st64(kin0 + 8u * (uint32_t)m,
@@ -191,48 +250,77 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
         hs::cluster_arrive();  // barrier A
 
         // ------------------------------------------------------------ phase 2
-        // every row whose gathered position is known: pool rows for hits, host
-        // rows for misses (placed into their slots after barrier B), zeros
+        const int nm = s_misc[0];
         if (gath) {
+            // every gathered row whose bytes are at hand: pool rows for hits,
+            // host rows for the misses this CTA reads (its claimed occurrences),
+            // zeros for absent entries. Host and pool loads share each round.
+            // Other occurrences of a union's miss copy their reader's row in
+            // phase 3.
             const int nunits = nloc * V;
             uint8_t *gdst = gathered + row0 * RB;
-            for (int base = tid; base < nunits; base += NT * UNROLL) {
-                uint4 v[UNROLL];
+            for (int base = tid; base < nunits; base += NT * UNROLL_H) {
+                uint4 v[UNROLL_H];
+                bool w[UNROLL_H];
 #pragma unroll
-                for (int u = 0; u < UNROLL; ++u) {
+                for (int u = 0; u < UNROLL_H; ++u) {
                     const int i = base + u * NT;
                     v[u] = make_uint4(0, 0, 0, 0);
+                    w[u] = false;
                     if (i < nunits) {
                         const int l = i / V, part = i - l * V;
                         const int kd = s_kind[l];
-                        if (kd == KIND_RES || kd == KIND_HOT)
+                        if (kd == KIND_RES || kd == KIND_HOT) {
                             v[u] = hs::ld_stream_v4(P.rows + (size_t)s_src[l] * RB + part * 16);
-                        else if (kd == KIND_MISS)
-                            v[u] = hs::ld_v4(P.host_rows + (size_t)s_hrow[l] * RB + part * 16);
+                            w[u] = true;
+                        } else if (kd == KIND_MISS) {
+                            if (s_claim[l] == j0 + l) {
+                                v[u] = hs::ld_v4(P.host_rows + (size_t)s_hrow[l] * RB + part * 16);
+                                w[u] = true;
+                            }
+                        } else {
+                            w[u] = true;
+                        }
                     }
                 }
 #pragma unroll
-                for (int u = 0; u < UNROLL; ++u)
-                    if (base + u * NT < nunits) hs::st_v4(gdst + (size_t)(base + u * NT) * 16, v[u]);
+                for (int u = 0; u < UNROLL_H; ++u)
+                    if (w[u]) hs::st_v4(gdst + (size_t)(base + u * NT) * 16, v[u]);
+            }
+        } else {
+            // rows stay in the pool: each miss row this CTA reads goes to
+            // shared memory until its slot is known (rows beyond the staging
+            // room are read again in phase 3)
+            for (int base = tid; base < nm * V; base += NT * UNROLL_H) {
+                uint4 v[UNROLL_H];
+                int at[UNROLL_H];  // staging unit, -1 = none
+#pragma unroll
+                for (int u = 0; u < UNROLL_H; ++u) {
+                    const int i = base + u * NT;
+                    at[u] = -1;
+                    if (i < nm * V) {
+                        const int mi = i / V, part = i - mi * V;
+                        const int l = s_mj[mi];
+                        const int st = (s_kind[l] >> 4) - 1;
+                        if (st >= 0) {
+                            v[u] = hs::ld_v4(P.host_rows + (size_t)s_hrow[l] * RB + part * 16);
+                            at[u] = st * V + part;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < UNROLL_H; ++u)
+                    if (at[u] >= 0) st_shared_v4(s_stage + (size_t)at[u] * 16, v[u]);
             }
         }
-        {
-            for (int l = tid; l < nloc; l += NT) {
-                const int kd = s_kind[l];
-                // in place, miss rows are read only after placement: start
-                // pulling them over the host link into L2 now
-                if (!gath && kd == KIND_MISS)
-                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
-                                     P.host_rows + (size_t)s_hrow[l] * RB),
-                                 "r"((uint32_t)RB)
-                                 : "memory");
-                if (kd != KIND_MISS) resolved[row0 + l] = kd == KIND_NONE ? -1 : s_src[l];
-                if (gath && fp8) {
-                    float sc = 0.f;
-                    if (kd == KIND_RES || kd == KIND_HOT) sc = P.scales[s_src[l]];
-                    else if (kd == KIND_MISS) sc = P.host_scales[s_hrow[l]];
-                    gscale[row0 + l] = sc;
-                }
+        for (int l = tid; l < nloc; l += NT) {
+            const int kd = s_kind[l] & 15;
+            if (kd != KIND_MISS) resolved[row0 + l] = kd == KIND_NONE ? -1 : s_src[l];
+            if (gath && fp8) {
+                float sc = 0.f;
+                if (kd == KIND_RES || kd == KIND_HOT) sc = P.scales[s_src[l]];
+                else if (kd == KIND_MISS) sc = P.host_scales[s_hrow[l]];
+                gscale[row0 + l] = sc;
             }
         }
         hs::cluster_wait();    // barrier A (long complete)
@@ -240,42 +328,62 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
         hs::cluster_wait();    // barrier B: rank 0 has placed every miss
 
         // ------------------------------------------------------------ phase 3
-        // placed miss rows: gathered -> hot slot (in place: host -> hot slot);
-        // rejected ones: zeroed in the gathered buffer
+        // Each placed position's row goes into its hot slot once, written by
+        // the occurrence that read it (from shared memory, or the gathered
+        // buffer / host arena when it was not staged); every other occurrence
+        // of a union takes the row id (and, with gathered rows, copies the
+        // reader's gathered row into its own). Rejected entries: zeros.
         {
-            __syncthreads();  // this CTA's gathered writes are visible to all its threads
-            const int nm = s_misc[0];
-            const int nunits = nm * V;
-            uint8_t *gsrc = gath ? gathered + row0 * RB : nullptr;
-            for (int base = tid; base < nunits; base += NT * UNROLL) {
+            const uint8_t *greq = gath ? gathered + (size_t)bi * K * RB : nullptr;
+            for (int base = tid; base < nm * V; base += NT * UNROLL) {
                 uint4 v[UNROLL];
-                int dst[UNROLL], l_[UNROLL], part_[UNROLL];
+                size_t slot[UNROLL], gdst[UNROLL];
+                bool tos[UNROLL], tog[UNROLL];
 #pragma unroll
                 for (int u = 0; u < UNROLL; ++u) {
                     const int i = base + u * NT;
-                    dst[u] = -2;
-                    if (i < nunits) {
+                    tos[u] = tog[u] = false;
+                    slot[u] = 0;
+                    gdst[u] = 0;
+                    if (i < nm * V) {
                         const int mi = i / V, part = i - mi * V;
                         const int l = s_mj[mi];
-                        l_[u] = l;
-                        part_[u] = part;
-                        dst[u] = s_src[l];
-                        if (dst[u] >= 0)
-                            v[u] = gath ? hs::ld_v4(gsrc + (size_t)l * RB + part * 16)
-                                        : hs::ld_v4(P.host_rows + (size_t)s_hrow[l] * RB + part * 16);
+                        const int cj = s_claim[l];
+                        const int d = s_src[l];
+                        const bool own = cj == j0 + l;
+                        const int sl = d >= 0 ? d : (d <= -2 ? -2 - d : -1);
+                        const int st = (s_kind[l] >> 4) - 1;
+                        gdst[u] = (row0 + l) * RB + part * 16;
+                        slot[u] = (size_t)(sl < 0 ? 0 : sl) * RB + part * 16;
+                        if (sl >= 0 && own) {
+                            tos[u] = true;
+                            v[u] = gath     ? hs::ld_v4(greq + (size_t)cj * RB + part * 16)
+                                 : st >= 0 ? ld_shared_v4(s_stage + (size_t)st * RB + part * 16)
+                                           : hs::ld_v4(P.host_rows + (size_t)s_hrow[l] * RB + part * 16);
+                        } else if (gath && sl >= 0) {
+                            tog[u] = true;
+                            v[u] = hs::ld_v4(greq + (size_t)cj * RB + part * 16);
+                        } else if (gath && sl < 0) {
+                            tog[u] = true;
+                            v[u] = make_uint4(0, 0, 0, 0);
+                        }
                     }
                 }
 #pragma unroll
                 for (int u = 0; u < UNROLL; ++u) {
-                    if (dst[u] >= 0)
-                        hs::st_v4(P.rows + (size_t)dst[u] * RB + part_[u] * 16, v[u]);
-                    else if (dst[u] == -1 && gath)
-                        hs::st_v4(gsrc + (size_t)l_[u] * RB + part_[u] * 16, make_uint4(0, 0, 0, 0));
+                    if (tos[u]) hs::st_v4(P.rows + (size_t)slot[u], v[u]);
+                    if (tog[u]) hs::st_v4(gathered + gdst[u], v[u]);
                 }
             }
             for (int mi = tid; mi < nm; mi += NT) {
                 const int l = s_mj[mi];
                 const int d = s_src[l];
+                if (d <= -2) {
+                    // a union's repeat: the row its first occurrence placed
+                    // (gathered row and scale already hold the host's bytes)
+                    resolved[row0 + l] = -2 - d;
+                    continue;
+                }
                 resolved[row0 + l] = d;
                 if (fp8) {
                     if (!gath) {
@@ -341,7 +449,8 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
                     first = (i == 0) || ((s_keys[i] >> 32) != (s_keys[i - 1] >> 32));
                 int tot;
                 const int pre = hs::block_scan_flag<NT>(first, s_warp, tot);
-                if (i < n_miss) s_rank[i] = first ? m + pre : -1;
+                // union of lists: a repeat takes its first occurrence's rank
+                if (i < n_miss) s_rank[i] = first ? m + pre : (uni ? m + pre - 1 : -1);
                 m += tot;
             }
             // stage the LRU order with each slot's protection in shared memory
@@ -393,30 +502,41 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
                 nu += tot;
             }
             const int mvict = min(mv, nu);
-            served = mvict;
             __syncthreads();
-            // place the misses; tell each owner worker its slot row (-1 = rejected)
+            // place the misses; tell each owner worker its slot row (-1 =
+            // rejected; in a union, -2 - row = a repeat of a placed miss, whose
+            // row the first occurrence copies)
+            if (tid == 0) s_misc[3] = 0;
+            __syncthreads();
+            int placed = 0;
             for (int i = tid; i < n_miss; i += NT) {
                 const unsigned long long key = s_keys[i];
                 const int p = static_cast<int>(key >> 32), j = static_cast<int>(key & 0xffffffffu);
                 const int rk = s_rank[i];
+                const bool first = (i == 0) || ((s_keys[i - 1] >> 32) != (key >> 32));
                 int dst = -1;
                 if (rk < 0) {
                     err |= HS_DEVERR_DUPLICATE;
                 } else if (rk >= mvict) {
                     err |= HS_DEVERR_CAPACITY;
+                    if (uni && first) p2s[p] = -1;  // drop the workers' mark
                 } else {
                     const int v = s_victim[rk];
-                    const int old = tag[v];
-                    if (old >= 0) p2s[old] = -1;
-                    tag[v] = p;
-                    stamp[v] = c;
-                    p2s[p] = v;
+                    if (first) {
+                        const int old = tag[v];
+                        if (old >= 0) p2s[old] = -1;
+                        tag[v] = p;
+                        stamp[v] = c;
+                        p2s[p] = v;
+                    }
                     dst = hblk[v >> 6] * hs::kPage + (v & 63);
+                    ++placed;
+                    if (!first) dst = -2 - dst;
                 }
                 const int owner = 1 + j / chunk;
                 hs::dsmem_st(hs::dsmem_map(&s_src[j - (owner - 1) * chunk], owner), dst);
             }
+            if (placed) atomicAdd(&s_misc[3], placed);
             __syncthreads();
             // the slots stamped this step, in slot order, close the LRU order
             int out = nu - mvict;
@@ -428,6 +548,7 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
                 if (f) lru[out + pre] = s;
                 out += tot;
             }
+            served = s_misc[3];  // misses resolved, counting the repeats of a union
         }
         if (tid == 0) {
             P.clock[r] = c;
@@ -453,16 +574,18 @@ int pick_cluster(int K) {
 
 }  // namespace
 
-size_t hs_resolve_smem_bytes(int K, int G, int C) {
+size_t hs_resolve_smem_bytes(int K, int G, int C, int RB, bool stage) {
     const int chunk = (K + G - 2) / (G - 1);
     Smem L{chunk, next_pow2(K), K, C, G - 1};
-    return L.total();
+    const size_t want = stage ? std::min(kStageSmemCap, L.off_kin() + (size_t)chunk * RB) : 0;
+    return (std::max(L.total(), want) + 15) & ~size_t(15);
 }
 
 hs_status hs_resolve_prepare(hs_pool *pool) {
     size_t mx = 0;
     for (int K = 1; K <= pool->cfg.max_topk; ++K) {
-        const size_t b = hs_resolve_smem_bytes(K, pick_cluster(K), pool->cfg.hot_rows);
+        const size_t b = hs_resolve_smem_bytes(K, pick_cluster(K), pool->cfg.hot_rows,
+                                               pool->row_bytes, true);
         if (b > mx) mx = b;
     }
     if (mx > 232448) return HS_ERR_UNSUPPORTED;  // shared memory per block on sm_103
@@ -475,10 +598,11 @@ hs_status hs_resolve_prepare(hs_pool *pool) {
 
 hs_status hs_launch_resolve(hs_pool *pool, int32_t B, const int32_t *req_ids, const int32_t *topk,
                             int32_t K, int32_t *resolved, void *gathered, float *gscale,
-                            int32_t *counts, cudaStream_t stream) {
+                            int32_t *counts, cudaStream_t stream, int uni) {
     const int G = pick_cluster(K);
     const int chunk = (K + G - 2) / (G - 1);
-    const size_t smem = hs_resolve_smem_bytes(K, G, pool->cfg.hot_rows);
+    const size_t smem =
+        hs_resolve_smem_bytes(K, G, pool->cfg.hot_rows, pool->row_bytes, gathered == nullptr);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G, B, 1);
     cfg.blockDim = dim3(NT, 1, 1);
@@ -495,20 +619,23 @@ hs_status hs_launch_resolve(hs_pool *pool, int32_t B, const int32_t *req_ids, co
     cudaError_t e;
     if (pool->row_bytes == 1152)
         e = cudaLaunchKernelEx(&cfg, resolve_kernel<1152>, P, req_ids, topk, (int)K, chunk, G,
-                               resolved, static_cast<uint8_t *>(gathered), gscale, counts);
+                               resolved, static_cast<uint8_t *>(gathered), gscale, counts, uni);
     else
         e = cudaLaunchKernelEx(&cfg, resolve_kernel<576>, P, req_ids, topk, (int)K, chunk, G,
-                               resolved, static_cast<uint8_t *>(gathered), gscale, counts);
+                               resolved, static_cast<uint8_t *>(gathered), gscale, counts, uni);
     return e == cudaSuccess ? HS_OK : HS_ERR_CUDA;
 }
 
-extern "C" hs_status hs_resolve_topk(hs_pool_t pool, int32_t B, const int32_t *d_req_ids,
-                                     const int32_t *d_topk_idx, int32_t K, int32_t *d_resolved,
-                                     void *d_gathered, float *d_gathered_scale, int32_t *d_counts,
-                                     void *stream) {
+namespace {
+hs_status resolve_entry(hs_pool_t pool, int32_t B, const int32_t *d_req_ids,
+                        const int32_t *d_topk_idx, int32_t K, int32_t *d_resolved,
+                        void *d_gathered, float *d_gathered_scale, int32_t *d_counts,
+                        void *stream, int uni) {
     if (!pool || B < 0 || !d_req_ids || !d_topk_idx || !d_resolved || !d_counts)
         return HS_ERR_INVALID_ARG;
-    if (K < 1 || K > pool->cfg.max_topk || K > pool->cfg.hot_rows) return HS_ERR_CAPACITY;
+    // one list: at most one entry per slot; a union: its distinct misses are
+    // checked against the free slots on the device
+    if (K < 1 || K > pool->cfg.max_topk || (!uni && K > pool->cfg.hot_rows)) return HS_ERR_CAPACITY;
     if (B > 65535) return HS_ERR_INVALID_ARG;
     const bool fp8 = pool->cfg.dtype == HS_FP8_E4M3_ROWSCALE;
     // gathered rows (and, for FP8 pools, their scales) or neither
@@ -517,5 +644,25 @@ extern "C" hs_status hs_resolve_topk(hs_pool_t pool, int32_t B, const int32_t *d
     if ((reinterpret_cast<uintptr_t>(d_gathered) & 15u) != 0) return HS_ERR_INVALID_ARG;
     if (B == 0) return HS_OK;
     return hs_launch_resolve(pool, B, d_req_ids, d_topk_idx, K, d_resolved, d_gathered,
-                             d_gathered_scale, d_counts, static_cast<cudaStream_t>(stream));
+                             d_gathered_scale, d_counts, static_cast<cudaStream_t>(stream), uni);
+}
+}  // namespace
+
+extern "C" hs_status hs_resolve_topk(hs_pool_t pool, int32_t B, const int32_t *d_req_ids,
+                                     const int32_t *d_topk_idx, int32_t K, int32_t *d_resolved,
+                                     void *d_gathered, float *d_gathered_scale, int32_t *d_counts,
+                                     void *stream) {
+    return resolve_entry(pool, B, d_req_ids, d_topk_idx, K, d_resolved, d_gathered,
+                         d_gathered_scale, d_counts, stream, 0);
+}
+
+// Several top-K lists per request (one per speculative query token) resolved
+// as their union against the request's one hot state.
+extern "C" hs_status hs_resolve_topk_union(hs_pool_t pool, int32_t B, const int32_t *d_req_ids,
+                                           const int32_t *d_topk_idx, int32_t K,
+                                           int32_t *d_resolved, void *d_gathered,
+                                           float *d_gathered_scale, int32_t *d_counts,
+                                           void *stream) {
+    return resolve_entry(pool, B, d_req_ids, d_topk_idx, K, d_resolved, d_gathered,
+                         d_gathered_scale, d_counts, stream, 1);
 }

@@ -263,6 +263,34 @@ def topk_lists(w: Workload) -> Iterator[np.ndarray]:
         raise ValueError(w.topk_kind)
 
 
+def token_lists(w: Workload, base: np.ndarray, step: int, fresh: float = 0.1) -> np.ndarray:
+    """One top-K list per query token for one decode step: int32 [B][T][K].
+
+    Token 0 keeps the step's list `base` ([B][K]); token t >= 1 (query position
+    L - T + t) keeps it too except for round(fresh*K) entries, at seeded random
+    indices, replaced by distinct positions drawn uniformly from [0, L - T + t]
+    that are not already in that token's list. Lists of different tokens
+    therefore overlap in about (1 - fresh) of their entries."""
+    rng = np.random.Generator(np.random.PCG64([w.seed, 7, step]))
+    B, K = base.shape
+    L = w.ctx
+    n_new = int(round(fresh * K))
+    out = np.empty((B, w.T, K), np.int32)
+    taken = np.zeros(L, dtype=bool)
+    for r in range(B):
+        out[r, 0] = base[r]
+        for t in range(1, w.T):
+            lst = base[r].copy()
+            idx = rng.choice(K, size=n_new, replace=False)
+            taken[lst] = True
+            new = _uniform_distinct(rng, 0, L - w.T + t + 1, n_new, taken)
+            taken[lst] = False
+            taken[new] = False
+            lst[idx] = new
+            out[r, t] = lst
+    return out
+
+
 # ------------------------------------------------------------------ rows, q
 def fill_rows(dtype: str, rows, scales, seed: int, chunk_rows: int = 1 << 20, gen_device=None):
     """Fill `rows` (torch uint8 [n, row_bytes], any device) with N(0,1) latent rows.
