@@ -50,29 +50,38 @@ constexpr int UNROLL = 4;     // 16-byte vectors in flight per thread and round
 constexpr int UNROLL_H = 8;   // the same for loops that read rows over the host link
 constexpr int KIND_NONE = 0, KIND_RES = 1, KIND_HOT = 2, KIND_MISS = 3;
 
-// Dynamic shared memory layout (bytes), identical in every CTA.
+// Dynamic shared memory layout (bytes), identical in every CTA. Rank 0 holds
+// no list entries, so its part overlaps the workers' part.
 struct Smem {
-    int chunk, kpad, K, C, W;  // W = workers = G - 1
+    int chunk, kpad, K, C;
+    // misc: [0] local misses, [1] resident, [2] hot, [3] staged rows (workers)
+    //       or placed misses (rank 0), [4] keys received (rank 0), [8..9]
+    //       totals, [20..52) warp scan scratch, [64 + 4g + 0..2] {misses,
+    //       resident, hot} of worker g (rank 0)
+    __host__ __device__ size_t off_misc() const { return 0; }
     // worker part
-    __host__ __device__ size_t off_src() const { return 0; }
+    __host__ __device__ size_t off_src() const { return 512; }
     __host__ __device__ size_t off_hrow() const { return off_src() + 4 * (size_t)chunk; }
     __host__ __device__ size_t off_kind() const { return off_hrow() + 4 * (size_t)chunk; }
     __host__ __device__ size_t off_mj() const { return off_kind() + 4 * (size_t)chunk; }
     // claim: for a miss, the request-level list index of the occurrence that
     // reads its row from the host (itself, unless a union repeats the position)
     __host__ __device__ size_t off_claim() const { return off_mj() + 4 * (size_t)chunk; }
-    // misc: [0] local misses, [1..3] worker totals, [20..52) warp scan scratch,
-    //       [64 + 4g + 0..2] {misses, resident, hot} of worker g (rank 0 only)
-    __host__ __device__ size_t off_misc() const { return off_claim() + 4 * (size_t)chunk; }
-    // rank-0 part
-    __host__ __device__ size_t off_kin() const { return (off_misc() + 4 * 128 + 15) & ~size_t(15); }
-    __host__ __device__ size_t off_keys() const { return off_kin() + 8 * (size_t)W * chunk; }
-    __host__ __device__ size_t off_rank() const { return off_keys() + 8 * (size_t)kpad; }
-    __host__ __device__ size_t off_victim() const { return off_rank() + 4 * (size_t)K; }
-    // victims: one per distinct miss, at most one per slot
+    // rows read from the host wait here for their slot (rows kept in the pool)
+    __host__ __device__ size_t off_stage() const {
+        return (off_claim() + 4 * (size_t)chunk + 15) & ~size_t(15);
+    }
+    // rank-0 part: miss keys (position << 32 | rank+1 << 13 | list index), the
+    // victims (one per distinct miss, at most one per slot), the LRU order and
+    // each slot's protection
+    __host__ __device__ size_t off_keys() const { return 512; }
+    __host__ __device__ size_t off_victim() const { return off_keys() + 8 * (size_t)kpad; }
     __host__ __device__ size_t off_lru() const { return off_victim() + 4 * (size_t)(K < C ? K : C); }
     __host__ __device__ size_t off_prot() const { return off_lru() + 4 * (size_t)C; }
-    __host__ __device__ size_t total() const { return off_prot() + (size_t)C; }
+    __host__ __device__ size_t total() const {
+        const size_t r0 = off_prot() + (size_t)C;
+        return r0 > off_stage() ? r0 : off_stage();
+    }
 };
 
 __host__ __device__ inline int next_pow2(int x) {
@@ -83,6 +92,12 @@ __host__ __device__ inline int next_pow2(int x) {
 
 __device__ __forceinline__ void dsmem_st64(uint32_t a, unsigned long long v) {
     asm volatile("st.shared::cluster.u64 [%0], %1;\n" ::"r"(a), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ int dsmem_atom_add(uint32_t a, int v) {
+    int r;
+    asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;\n" : "=r"(r) : "r"(a), "r"(v) : "memory");
+    return r;
 }
 
 __device__ __forceinline__ void st_shared_v4(void *p, uint4 v) {
@@ -108,12 +123,114 @@ __device__ __forceinline__ uint32_t dyn_smem_bytes() {
     return n;
 }
 
+// ---------------------------------------------------------------- key sort
+// Bitonic sort of up to 4096 64-bit keys held in registers, 8 per thread
+// (element e = 8t + r of thread t). Strides below 8 pair registers of one
+// thread, strides 8..128 pair threads of one warp (shuffles), larger strides
+// go through shared memory. Element e lives in shared memory at swz(e), which
+// spreads a warp's accesses over the banks.
+__device__ __forceinline__ int swz8(int e) { return (e & ~7) | ((e ^ (e >> 3)) & 7); }
+
+__device__ __forceinline__ void cmpx(unsigned long long &a, unsigned long long &b, bool asc) {
+    const bool sw = (a > b) == asc;
+    const unsigned long long lo = sw ? b : a, hi = sw ? a : b;
+    a = lo;
+    b = hi;
+}
+
+template <int JJ>
+__device__ __forceinline__ void reg_stage(unsigned long long (&x)[8], int t, int k) {
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+        if ((r & JJ) == 0) cmpx(x[r], x[r | JJ], ((t * 8 + r) & k) == 0);
+}
+
+// s: the keys at swz(e), e < n2 (a power of two, 8 <= n2 <= 8 * NT); sorted in place.
+__device__ __noinline__ void sort_keys_reg(unsigned long long *s, int n2, int tid) {
+    const int T = n2 >> 3;  // threads holding keys
+    const bool act = tid < T;
+    unsigned long long x[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) x[r] = act ? s[swz8(tid * 8 + r)] : ~0ull;
+    for (int k = 2; k <= n2; k <<= 1) {
+        for (int jj = k >> 1; jj > 0; jj >>= 1) {
+            if (jj >= 256) {
+                __syncthreads();  // previous readers of s are done
+                if (act) {
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) s[swz8(tid * 8 + r)] = x[r];
+                }
+                __syncthreads();
+                if (act) {
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        const int e = tid * 8 + r;
+                        const unsigned long long y = s[swz8(e ^ jj)];
+                        const bool keep_min = ((e & jj) == 0) == ((e & k) == 0);
+                        x[r] = keep_min ? (x[r] < y ? x[r] : y) : (x[r] > y ? x[r] : y);
+                    }
+                }
+            } else if (jj >= 8) {
+                const int m = jj >> 3;  // partner lane offset (xor)
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int e = tid * 8 + r;
+                    const unsigned lo = __shfl_xor_sync(0xffffffffu, (unsigned)x[r], m);
+                    const unsigned hi = __shfl_xor_sync(0xffffffffu, (unsigned)(x[r] >> 32), m);
+                    const unsigned long long y = ((unsigned long long)hi << 32) | lo;
+                    const bool keep_min = ((e & jj) == 0) == ((e & k) == 0);
+                    x[r] = keep_min ? (x[r] < y ? x[r] : y) : (x[r] > y ? x[r] : y);
+                }
+            } else if (jj == 4) {
+                reg_stage<4>(x, tid, k);
+            } else if (jj == 2) {
+                reg_stage<2>(x, tid, k);
+            } else {
+                reg_stage<1>(x, tid, k);
+            }
+        }
+    }
+    __syncthreads();
+    if (act) {
+#pragma unroll
+        for (int r = 0; r < 8; ++r) s[swz8(tid * 8 + r)] = x[r];
+    }
+    __syncthreads();
+}
+
+// The same sort for any power-of-two count, by a shared-memory bitonic
+// network, keys stored at e. A pair of a stage with stride jj <= 32 stays
+// inside the 64 keys of its 32-aligned group of pairs, which one warp owns
+// across such stages: those stages sync the warp only.
+__device__ __forceinline__ void sort_keys_smem(unsigned long long *s, int n2, int tid) {
+    for (int k = 2; k <= n2; k <<= 1) {
+        for (int jj = k >> 1; jj > 0; jj >>= 1) {
+            for (int i = tid; i < (n2 >> 1); i += NT) {
+                const int lo = ((i & ~(jj - 1)) << 1) | (i & (jj - 1)), hi = lo + jj;
+                const unsigned long long a = s[lo], b = s[hi];
+                if ((a > b) == ((lo & k) == 0)) {
+                    s[lo] = b;
+                    s[hi] = a;
+                }
+            }
+            const int next = jj > 1 ? jj >> 1 : k;  // stride of the next stage
+            if (jj >= 64 || next >= 64)
+                __syncthreads();
+            else
+                __syncwarp();
+        }
+    }
+    __syncthreads();
+}
+
 // Dynamic shared memory of a launch: the layout; with rows kept in the pool,
 // grown (while two CTAs still fit on an SM) so that a worker can stage every
 // row of its share of the list.
 constexpr size_t kStageSmemCap = 110 * 1024;
 
-template <int RB>
+// BIG: lists longer than 2048 entries (up to 4096 misses sort in registers).
+// Shorter lists use the kernel without that path, which holds fewer registers.
+template <int RB, bool BIG>
 __global__ void __launch_bounds__(NT, 2)
 resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
                const int32_t *__restrict__ topk, int K, int chunk, int G,
@@ -122,7 +239,7 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
     constexpr int V = RB / 16;  // 16-byte vectors per row
     extern __shared__ __align__(16) unsigned char smem[];
     const int W = G - 1;
-    const Smem L{chunk, next_pow2(K), K, P.C, W};
+    const Smem L{chunk, max(8, next_pow2(K)), K, P.C};
     int32_t *s_src = reinterpret_cast<int32_t *>(smem + L.off_src());
     int32_t *s_hrow = reinterpret_cast<int32_t *>(smem + L.off_hrow());
     int32_t *s_kind = reinterpret_cast<int32_t *>(smem + L.off_kind());
@@ -131,16 +248,14 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
     int32_t *s_misc = reinterpret_cast<int32_t *>(smem + L.off_misc());
     int32_t *s_warp = s_misc + 20;
     int32_t *s_wcnt = s_misc + 64;  // [G][4], filled by the workers (rank 0 only)
-    unsigned long long *s_kin = reinterpret_cast<unsigned long long *>(smem + L.off_kin());
     unsigned long long *s_keys = reinterpret_cast<unsigned long long *>(smem + L.off_keys());
-    int32_t *s_rank = reinterpret_cast<int32_t *>(smem + L.off_rank());
     int32_t *s_victim = reinterpret_cast<int32_t *>(smem + L.off_victim());
     int32_t *s_lru = reinterpret_cast<int32_t *>(smem + L.off_lru());
     uint8_t *s_prot = smem + L.off_prot();
-    // workers: the rank-0 part of their own shared memory stages the miss rows
-    // they read from the host (rows beyond its capacity are read directly)
-    uint8_t *s_stage = smem + L.off_kin();
-    const int ncap = static_cast<int>((dyn_smem_bytes() - L.off_kin()) / RB);
+    // workers: the end of their shared memory stages the miss rows they read
+    // from the host (rows beyond its capacity are read directly)
+    uint8_t *s_stage = smem + L.off_stage();
+    const int ncap = static_cast<int>((dyn_smem_bytes() - L.off_stage()) / RB);
 
     const int tid = threadIdx.x;
     const int g = static_cast<int>(hs::cluster_ctarank());
@@ -176,7 +291,7 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
     int32_t *lru = P.lru + (size_t)r * C;
     int32_t *p2s = P.p2s + (size_t)r * P.max_ctx;
 
-    if (tid == 0) s_misc[0] = s_misc[1] = s_misc[2] = s_misc[3] = 0;
+    if (tid == 0) s_misc[0] = s_misc[1] = s_misc[2] = s_misc[3] = s_misc[4] = 0;
     // every CTA of the cluster is running (and has set up its shared memory)
     // before any distributed-shared-memory store below
     __syncthreads();
@@ -186,12 +301,17 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
     uint32_t err = 0;
     if (g != 0) {
         // ------------------------------------------------------------ phase 1
-        const uint32_t kin0 = hs::dsmem_map(s_kin + (size_t)(g - 1) * chunk, 0);
+        // keys go straight into rank 0's key array, at slots taken (one remote
+        // atomic per warp) from its counter
+        const uint32_t keys0 = hs::dsmem_map(s_keys, 0);
+        const uint32_t nkeys0 = hs::dsmem_map(&s_misc[4], 0);
+        const int lane = tid & 31;
         int n_res = 0, n_hot = 0;
-        for (int l = tid; l < nloc; l += NT) {
-            const int p = topk[row0 + l];
+        for (int lb = 0; lb < nloc; lb += NT) {  // warp-uniform trip count
+            const int l = lb + tid;
+            const int p = l < nloc ? topk[row0 + l] : -1;
             int kind = KIND_NONE, src = -1, hrow = -1;
-            if (p == -1) {
+            if (l >= nloc || p == -1) {
             } else if (p < 0 || p >= Lr || p >= P.max_ctx) {
                 err |= HS_DEVERR_INDEX_RANGE;
             } else {
@@ -231,14 +351,25 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
                         }
                         const int m = atomicAdd(&s_misc[0], 1);
                         s_mj[m] = l;
-                        dsmem_st64(kin0 + 8u * (uint32_t)m,
-                                   ((unsigned long long)(uint32_t)p << 32) | (uint32_t)(j0 + l));
                     }
                 }
             }
-            s_kind[l] = kind;
-            s_src[l] = src;
-            s_hrow[l] = hrow;
+            const bool miss = (kind & 15) == KIND_MISS;
+            const unsigned bal = __ballot_sync(0xffffffffu, miss);
+            if (bal) {
+                const int leader = __ffs(bal) - 1;
+                int kb = 0;
+                if (lane == leader) kb = dsmem_atom_add(nkeys0, __popc(bal));
+                kb = __shfl_sync(0xffffffffu, kb, leader);
+                if (miss)
+                    dsmem_st64(keys0 + 8u * (uint32_t)(kb + __popc(bal & ((1u << lane) - 1u))),
+                               ((unsigned long long)(uint32_t)p << 32) | (uint32_t)(j0 + l));
+            }
+            if (l < nloc) {
+                s_kind[l] = kind;
+                s_src[l] = src;
+                s_hrow[l] = hrow;
+            }
         }
         if (n_res) atomicAdd(&s_misc[1], n_res);
         if (n_hot) atomicAdd(&s_misc[2], n_hot);
@@ -261,31 +392,30 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
             uint8_t *gdst = gathered + row0 * RB;
             for (int base = tid; base < nunits; base += NT * UNROLL_H) {
                 uint4 v[UNROLL_H];
-                bool w[UNROLL_H];
+                unsigned w = 0;  // bit u: store vector u
 #pragma unroll
                 for (int u = 0; u < UNROLL_H; ++u) {
                     const int i = base + u * NT;
                     v[u] = make_uint4(0, 0, 0, 0);
-                    w[u] = false;
                     if (i < nunits) {
                         const int l = i / V, part = i - l * V;
                         const int kd = s_kind[l];
                         if (kd == KIND_RES || kd == KIND_HOT) {
                             v[u] = hs::ld_stream_v4(P.rows + (size_t)s_src[l] * RB + part * 16);
-                            w[u] = true;
+                            w |= 1u << u;
                         } else if (kd == KIND_MISS) {
                             if (s_claim[l] == j0 + l) {
                                 v[u] = hs::ld_v4(P.host_rows + (size_t)s_hrow[l] * RB + part * 16);
-                                w[u] = true;
+                                w |= 1u << u;
                             }
                         } else {
-                            w[u] = true;
+                            w |= 1u << u;
                         }
                     }
                 }
 #pragma unroll
                 for (int u = 0; u < UNROLL_H; ++u)
-                    if (w[u]) hs::st_v4(gdst + (size_t)(base + u * NT) * 16, v[u]);
+                    if (w >> u & 1u) hs::st_v4(gdst + (size_t)(base + u * NT) * 16, v[u]);
             }
         } else {
             // rows stay in the pool: each miss row this CTA reads goes to
@@ -400,57 +530,51 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
         // ------------------------------------------------------------ rank 0
         hs::cluster_arrive();  // barrier A
         hs::cluster_wait();
-        int32_t *s_off = s_misc + 4;  // [0..W] miss offsets of the workers, then totals
         if (tid == 0) {
-            int acc = 0, res = 0, hot = 0;
+            int res = 0, hot = 0;
             for (int q = 1; q <= W; ++q) {
-                s_off[q - 1] = acc;
-                acc += s_wcnt[4 * q];
                 res += s_wcnt[4 * q + 1];
                 hot += s_wcnt[4 * q + 2];
             }
-            s_off[W] = acc;
-            s_off[W + 1] = res;
-            s_off[W + 2] = hot;
+            s_misc[8] = res;
+            s_misc[9] = hot;
         }
         __syncthreads();
-        const int n_miss = s_off[W], tot_res = s_off[W + 1], tot_hot = s_off[W + 2];
+        // the workers' keys are in s_keys[0, n_miss), in arrival order
+        const int n_miss = s_misc[4], tot_res = s_misc[8], tot_hot = s_misc[9];
         const bool leased = hblk[0] >= 0;
         int served = 0;
         if (n_miss > 0 || tot_hot > 0) {
-            // dense key array from the workers' regions
-            for (int q = 1; q <= W; ++q) {
-                const int nq = s_off[q] - s_off[q - 1];
-                for (int i = tid; i < nq; i += NT)
-                    s_keys[s_off[q - 1] + i] = s_kin[(size_t)(q - 1) * chunk + i];
-            }
-            const int n2 = next_pow2(n_miss);
+            // sort the keys by (position, list index), ascending. 4096 keys
+            // (a union of per-token lists): in registers, stored at swz8(i);
+            // otherwise in shared memory, stored at i. (Measured: the register
+            // network wins at 4096 keys and loses at 1024.)
+            const int n2 = max(8, next_pow2(n_miss));
             for (int i = n_miss + tid; i < n2; i += NT) s_keys[i] = ~0ull;
             __syncthreads();
-            for (int k = 2; k <= n2; k <<= 1) {  // bitonic sort, ascending
-                for (int jj = k >> 1; jj > 0; jj >>= 1) {
-                    for (int i = tid; i < (n2 >> 1); i += NT) {
-                        const int lo = ((i & ~(jj - 1)) << 1) | (i & (jj - 1)), hi = lo + jj;
-                        const unsigned long long a = s_keys[lo], b = s_keys[hi];
-                        if ((a > b) == ((lo & k) == 0)) {
-                            s_keys[lo] = b;
-                            s_keys[hi] = a;
-                        }
-                    }
-                    __syncthreads();
-                }
+            const bool regsort = BIG && n2 == 8 * NT;
+            if (regsort) {
+                sort_keys_reg(s_keys, n2, tid);
+            } else {
+                sort_keys_smem(s_keys, n2, tid);
             }
-            // rank of each miss among distinct positions; repeats get -1
+            // sorted key i sits at kat(i)
+            auto kat = [regsort](int i) { return regsort ? swz8(i) : i; };
+            // rank of each miss among distinct positions (repeats: none; in a
+            // union, their first occurrence's), stored as rank + 1 in key bits 13..26
             int m = 0;
             for (int base = 0; base < n_miss; base += NT) {
                 const int i = base + tid;
                 int first = 0;
                 if (i < n_miss)
-                    first = (i == 0) || ((s_keys[i] >> 32) != (s_keys[i - 1] >> 32));
+                    first = (i == 0) || ((s_keys[kat(i)] >> 32) != (s_keys[kat(i - 1)] >> 32));
                 int tot;
                 const int pre = hs::block_scan_flag<NT>(first, s_warp, tot);
-                // union of lists: a repeat takes its first occurrence's rank
-                if (i < n_miss) s_rank[i] = first ? m + pre : (uni ? m + pre - 1 : -1);
+                if (i < n_miss) {
+                    const int rk = first ? m + pre : (uni ? m + pre - 1 : -1);
+                    unsigned long long &key = s_keys[kat(i)];
+                    key = (key & ~0xffffffffull) | ((unsigned long long)(rk + 1) << 13) | (key & 0x1fffull);
+                }
                 m += tot;
             }
             // stage the LRU order with each slot's protection in shared memory
@@ -510,10 +634,10 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
             __syncthreads();
             int placed = 0;
             for (int i = tid; i < n_miss; i += NT) {
-                const unsigned long long key = s_keys[i];
-                const int p = static_cast<int>(key >> 32), j = static_cast<int>(key & 0xffffffffu);
-                const int rk = s_rank[i];
-                const bool first = (i == 0) || ((s_keys[i - 1] >> 32) != (key >> 32));
+                const unsigned long long key = s_keys[kat(i)];
+                const int p = static_cast<int>(key >> 32), j = static_cast<int>(key & 0x1fffu);
+                const int rk = static_cast<int>((key >> 13) & 0x3fffu) - 1;
+                const bool first = (i == 0) || ((s_keys[kat(i - 1)] >> 32) != (key >> 32));
                 int dst = -1;
                 if (rk < 0) {
                     err |= HS_DEVERR_DUPLICATE;
@@ -576,8 +700,8 @@ int pick_cluster(int K) {
 
 size_t hs_resolve_smem_bytes(int K, int G, int C, int RB, bool stage) {
     const int chunk = (K + G - 2) / (G - 1);
-    Smem L{chunk, next_pow2(K), K, C, G - 1};
-    const size_t want = stage ? std::min(kStageSmemCap, L.off_kin() + (size_t)chunk * RB) : 0;
+    Smem L{chunk, std::max(8, next_pow2(K)), K, C};
+    const size_t want = stage ? std::min(kStageSmemCap, L.off_stage() + (size_t)chunk * RB) : 0;
     return (std::max(L.total(), want) + 15) & ~size_t(15);
 }
 
@@ -589,9 +713,13 @@ hs_status hs_resolve_prepare(hs_pool *pool) {
         if (b > mx) mx = b;
     }
     if (mx > 232448) return HS_ERR_UNSUPPORTED;  // shared memory per block on sm_103
-    HS_CUDA_TRY(cudaFuncSetAttribute(resolve_kernel<1152>,
+    HS_CUDA_TRY(cudaFuncSetAttribute(resolve_kernel<1152, false>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx));
-    HS_CUDA_TRY(cudaFuncSetAttribute(resolve_kernel<576>,
+    HS_CUDA_TRY(cudaFuncSetAttribute(resolve_kernel<576, false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx));
+    HS_CUDA_TRY(cudaFuncSetAttribute(resolve_kernel<1152, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx));
+    HS_CUDA_TRY(cudaFuncSetAttribute(resolve_kernel<576, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx));
     return HS_OK;
 }
@@ -617,12 +745,18 @@ hs_status hs_launch_resolve(hs_pool *pool, int32_t B, const int32_t *req_ids, co
     cfg.numAttrs = 1;
     const hs::DevPool P = pool->dev();
     cudaError_t e;
+    auto *uc = static_cast<uint8_t *>(gathered);
+    const bool big = K > 2048;
     if (pool->row_bytes == 1152)
-        e = cudaLaunchKernelEx(&cfg, resolve_kernel<1152>, P, req_ids, topk, (int)K, chunk, G,
-                               resolved, static_cast<uint8_t *>(gathered), gscale, counts, uni);
+        e = big ? cudaLaunchKernelEx(&cfg, resolve_kernel<1152, true>, P, req_ids, topk, (int)K,
+                                     chunk, G, resolved, uc, gscale, counts, uni)
+                : cudaLaunchKernelEx(&cfg, resolve_kernel<1152, false>, P, req_ids, topk, (int)K,
+                                     chunk, G, resolved, uc, gscale, counts, uni);
     else
-        e = cudaLaunchKernelEx(&cfg, resolve_kernel<576>, P, req_ids, topk, (int)K, chunk, G,
-                               resolved, static_cast<uint8_t *>(gathered), gscale, counts, uni);
+        e = big ? cudaLaunchKernelEx(&cfg, resolve_kernel<576, true>, P, req_ids, topk, (int)K,
+                                     chunk, G, resolved, uc, gscale, counts, uni)
+                : cudaLaunchKernelEx(&cfg, resolve_kernel<576, false>, P, req_ids, topk, (int)K,
+                                     chunk, G, resolved, uc, gscale, counts, uni);
     return e == cudaSuccess ? HS_OK : HS_ERR_CUDA;
 }
 
