@@ -224,6 +224,9 @@ def run_gpu(args):
     per_token = bool(args.per_token)
     if per_token and (agent or w.T < 2):
         raise SystemExit("--per-token needs a workload with several query tokens (hybrid)")
+    L = max(1, args.layers)
+    if L > 1 and (agent or per_token):
+        raise SystemExit("--layers applies to the single-list workloads")
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         if agent:
@@ -239,6 +242,24 @@ def run_gpu(args):
                 # must read at least once)
                 uniq = [sum(len(np.unique(gw.topk_host[s][b][gw.topk_host[s][b] >= 0]))
                             for b in range(w.B)) for s in range(w.steps)]
+        gws, group = [gw], None
+        if L > 1:
+            # layers 1..L-1: pools of the same shape with their own seeds; one
+            # resolve launch covers all layers, each layer then decodes on its own
+            gws += [GpuWorkload(w.scaled(index=w.index + 100 * l), stream=stream,
+                                in_place=args.in_place) for l in range(1, L)]
+            res_all = torch.empty((L, w.B, w.K), dtype=torch.int32, device="cuda")
+            gat_all = (None if args.in_place else
+                       torch.empty((L, w.B, w.K, w.row_bytes), dtype=torch.uint8, device="cuda"))
+            gsc_all = (torch.empty((L, w.B, w.K), dtype=torch.float32, device="cuda")
+                       if (w.dtype == "fp8" and not args.in_place) else None)
+            cnt_all = torch.empty((L, w.B, 3), dtype=torch.int32, device="cuda")
+            for l, x in enumerate(gws):
+                x.resolved, x.counts = res_all[l], cnt_all[l]
+                x.gathered = None if gat_all is None else gat_all[l]
+                x.gscale = None if gsc_all is None else gsc_all[l]
+            lists = [torch.stack([x.topk[s] for x in gws]).contiguous() for s in range(w.steps)]
+            group = hs.hs_layer_group_create([x.pool for x in gws])
         nq = min(len(lists), 16)
         qs = [W.make_q(w, s, device="cuda") for s in range(nq)]
         flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
@@ -246,7 +267,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     if agent:
         gw.apply(plan[0])
-    snap = gw.pool.snapshot()
+    snaps = [x.pool.snapshot() for x in gws]
     n_lists = len(lists)
 
     def l2_flush():
@@ -261,7 +282,8 @@ def run_gpu(args):
         i = s % n_lists
         if i == 0 and s > 0:
             torch.cuda.synchronize()
-            gw.pool.restore(snap)
+            for x, sn in zip(gws, snaps):
+                x.pool.restore(sn)
         if agent:
             gw.apply(plan[i])
 
@@ -270,7 +292,10 @@ def run_gpu(args):
         q = qs[s % nq]
         if ev is not None:
             ev[0].record(stream)
-        if per_token:
+        if L > 1:
+            hs.hs_resolve_topk_layers(group, gw.req_ids, t, res_all, gat_all, gsc_all, cnt_all,
+                                      stream)
+        elif per_token:
             gw.pool.resolve_topk_union(gw.req_ids, t, gw.resolved, gw.gathered, gw.gscale,
                                        gw.counts, stream)
         else:
@@ -278,7 +303,11 @@ def run_gpu(args):
                                  stream)
         if ev is not None:
             ev[1].record(stream)
-        if per_token:
+        if L > 1:
+            for l, x in enumerate(gws):  # the layers' queries: the step's q, reused
+                x.pool.sparse_mla_decode(q, x.gathered, x.gscale, x.resolved, t[l], x.req_ids,
+                                         w.sm_scale, x.out, x.lse, x.workspace, stream)
+        elif per_token:
             gw.pool.sparse_mla_decode_per_token(q, gw.gathered, gw.gscale, gw.resolved, t,
                                                 gw.req_ids, w.sm_scale, gw.out, gw.lse,
                                                 gw.workspace, stream)
@@ -294,9 +323,10 @@ def run_gpu(args):
             l2_flush()
             step(s)
     torch.cuda.synchronize()
-    assert gw.pool.get_error() == 0
+    assert all(x.pool.get_error() == 0 for x in gws)
     # timed steps start from the beginning of the step list and its initial state
-    gw.pool.restore(snap)
+    for x, sn in zip(gws, snaps):
+        x.pool.restore(sn)
     if agent:
         gw.apply(plan[0])
 
@@ -320,7 +350,7 @@ def run_gpu(args):
                 tag_prev.copy_(slot_tag)
             l2_flush()
             step(s, evs[s])
-            counts_acc += gw.counts.sum(0)
+            counts_acc += cnt_all.sum((0, 1)) if L > 1 else gw.counts.sum(0)
             if per_token:
                 retagged += (slot_tag != tag_prev).sum()
         torch.cuda.nvtx.range_pop()
@@ -336,7 +366,7 @@ def run_gpu(args):
     steps_per_s = whole_job_rate(1.0, ws, ms_step)
     res_ms = sum(t_res) / steps
     dec_ms = sum(t_dec) / steps
-    rows_per_s = ws * w.B * w.K / (res_ms * 1e-3)
+    rows_per_s = ws * L * w.B * w.K / (res_ms * 1e-3)
 
     per_step_counts = cnt_sum / steps
     pt = None
@@ -344,7 +374,8 @@ def run_gpu(args):
         pt = (sum(uniq[s % n_lists] for s in range(steps)) / steps,
               float(retagged.item()) / steps)
         rows_per_s = ws * w.B * w.T * w.K / (res_ms * 1e-3)
-    r_hbm, r_link, d_bytes, flops = algorithmic(w, per_step_counts, args.in_place, pt)
+    r_hbm, r_link, d_bytes, flops = algorithmic(w, per_step_counts / L, args.in_place, pt)
+    r_hbm, r_link, d_bytes, flops = r_hbm * L, r_link * L, d_bytes * L, flops * L
     hbm_peak, tf_peak, peak_kind = _peaks()
     kernels = {
         "resolve": {"ms": res_ms, "achieved": r_hbm / (res_ms * 1e-3) / 1e9, "unit": "GB/s",
@@ -355,7 +386,7 @@ def run_gpu(args):
                    "tflops": flops / (dec_ms * 1e-3) / 1e12,
                    "traffic": _traffic("decode", "tiered_sparse_mla_gb300/csrc/hs_decode.cu")},
     }
-    if name != WORKLOAD or w.B != W.WORKLOADS[WORKLOAD].B:
+    if name != WORKLOAD or w.B != W.WORKLOADS[WORKLOAD].B or L > 1 or args.in_place or per_token:
         kernels["resolve"]["traffic"] = kernels["decode"]["traffic"] = None  # captured on another workload
     # the decode's roofline time is max(bytes / BW, flops / tensor peak)
     t_bytes = d_bytes / (hbm_peak * 1e9)
@@ -370,21 +401,24 @@ def run_gpu(args):
                 "frac": round(kt["achieved"] / kt["peak"], 4), "traffic": kt["traffic"],
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"}
 
-    launches = 2 + (1 if (hs.hs_decode_workspace_bytes(w.B * w.T, 1, w.H, w.K) if per_token else
-                          hs.hs_decode_workspace_bytes(w.B, w.T, w.H, w.K)) > 0 else 0)
+    launches = 1 + L * (1 + (1 if (hs.hs_decode_workspace_bytes(w.B * w.T, 1, w.H, w.K) if per_token
+                                   else hs.hs_decode_workspace_bytes(w.B, w.T, w.H, w.K)) > 0 else 0))
     desc = DESCS[name] if (agent or w.B == W.WORKLOADS[name].B) else f"{DESCS[name]} [batch {w.B}]"
     if not agent and w.ctx != W.WORKLOADS[name].ctx:
         desc += f" [context {w.ctx}]"
     if per_token:
         desc += (f" [one top-{w.K} list per query token (10% fresh per later token), the "
                  f"{w.T} lists of a request resolved as one union]")
+    if L > 1:
+        desc += (f" [{L} layers, each its own pool and lists: one resolve launch for all layers, "
+                 f"then one decode per layer]")
     line = {
         "metric": METRIC, "value": round(steps_per_s, 2), "unit": "decode steps/s",
         "n_gpus": ws, "steps": steps, "warmup": args.warmup,
         "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "fp8 rows, f16 MMA",
         "data": "synthetic",
-        "config": {"workload": desc, "global_batch": w.B * ws, "top_k": w.K,
+        "config": {"workload": desc, "global_batch": w.B * ws, "top_k": w.K, "layers": L,
                    "heads": w.H, "query_tokens": w.T, "ctx": w.ctx,
                    "parallelism": f"replicas x{ws} (requests sharded by rank, no collective)",
                    "rows": ("read in place from the pool by attention (no gathered buffer)"
@@ -417,13 +451,16 @@ def run_gpu(args):
             if a < b:
                 per_turn.append(round(sum(t_res[a:b]) + sum(t_dec[a:b]), 3))
         line["per_turn_ms"] = per_turn
-    if name == WORKLOAD and not agent:
+    if name == WORKLOAD and not agent and L == 1:
         line["e2e"] = run_e2e(args, gw, qs, stream, w)
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline and name == WORKLOAD:
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and name == WORKLOAD and L == 1:
         line["cpu_baseline"] = cpu_baseline(w, args)
     if rank == 0:
         print(json.dumps(line), flush=True)
-    gw.pool.close()
+    if group is not None:
+        hs.hs_layer_group_destroy(group)
+    for x in gws:
+        x.pool.close()
     if ws > 1:
         dist.destroy_process_group()
 
@@ -625,6 +662,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="requests per step (default: the workload's; smaller only for profiling)")
+    ap.add_argument("--layers", type=int, default=1,
+                    help="L layers (own pools and lists): one multi-layer resolve launch per step")
     ap.add_argument("--per-token", action="store_true",
                     help="one top-K list per query token: union resolve + per-token decode")
     ap.add_argument("--in-place", action="store_true",

@@ -35,6 +35,7 @@ extern "C" {
 #endif
 
 typedef struct hs_pool *hs_pool_t;
+typedef struct hs_layer_group *hs_layer_group_t;
 
 typedef enum {
     HS_OK = 0,
@@ -181,6 +182,28 @@ hs_status hs_resolve_topk_union(hs_pool_t pool, int32_t B, const int32_t *d_req_
                                 const int32_t *d_topk_idx, int32_t K, int32_t *d_resolved,
                                 void *d_gathered, float *d_gathered_scale, int32_t *d_counts,
                                 void *stream);
+
+/* Several sparse-MLA layers resolved in one launch ([A] 关键架构细节, 轻量级执行:
+ * all sparse-MLA layers are launched at once, in the model stream's order).
+ * Each layer has its own pool (rows, page table, hot buffers, LRU state); the
+ * pools of a group share dtype, hot_rows and max_topk and live on the current
+ * device. hs_layer_group_create copies the pools' table addresses to the
+ * device once (synchronous); the pools must outlive the group, which owns
+ * nothing else. */
+hs_status hs_layer_group_create(const hs_pool_t *pools, int32_t L, hs_layer_group_t *out);
+hs_status hs_layer_group_destroy(hs_layer_group_t group);
+
+/* hs_resolve_topk for every layer of a group in one launch: one cluster per
+ * (request, layer), each layer exactly as hs_resolve_topk would resolve it
+ * (its own clock, LRU state and error word).
+ *   d_req_ids [B] (the same requests in every layer); d_topk_idx and
+ *   d_resolved [L][B][K]; d_gathered [L][B][K][row_bytes] or NULL;
+ *   d_gathered_scale [L][B][K] (FP8 with gathered rows) or NULL;
+ *   d_counts [L][B][3]. Requires 1 <= K <= min(max_topk, hot_rows). */
+hs_status hs_resolve_topk_layers(hs_layer_group_t group, int32_t B, const int32_t *d_req_ids,
+                                 const int32_t *d_topk_idx, int32_t K, int32_t *d_resolved,
+                                 void *d_gathered, float *d_gathered_scale, int32_t *d_counts,
+                                 void *stream);
 
 /* Sparse MLA decode over the gathered rows: attention restricted to the K
  * selected latent rows (解决 KV 缓存内存压力; 稀疏MLA的核心思想). Query token t of request b sits at position L_b - T + t

@@ -226,3 +226,63 @@ def test_snapshot_restore_replays_identically():
     for k in outs[0][2]:
         assert np.array_equal(outs[0][2][k], outs[1][2][k])
     gw.pool.close()
+
+
+# ---------------------------------------------------------------- several layers, one launch
+def _run_layers(w, L, steps, in_place=False, nthreads=8):
+    """L layers (pools of the same shape, own seeds) resolved by one
+    hs_resolve_topk_layers launch per step; every layer is compared with its
+    own oracle exactly as a single-layer resolve is."""
+    import tiered_sparse_mla_gb300 as hs
+    from harness import GpuWorkload
+    from _mirror import compare_resolve, oracle_mirror
+    gws = [GpuWorkload(w.scaled(index=w.index + 100 * l), in_place=in_place) for l in range(L)]
+    ots = [oracle_mirror(gw) for gw in gws]
+    B, K, rb = w.B, w.K, w.row_bytes
+    res = torch.empty((L, B, K), dtype=torch.int32, device="cuda")
+    gat = None if in_place else torch.empty((L, B, K, rb), dtype=torch.uint8, device="cuda")
+    gsc = (torch.empty((L, B, K), dtype=torch.float32, device="cuda")
+           if (w.dtype == "fp8" and not in_place) else None)
+    cnt = torch.empty((L, B, 3), dtype=torch.int32, device="cuda")
+    for l, gw in enumerate(gws):  # per-layer views, read by compare_resolve
+        gw.resolved, gw.counts = res[l], cnt[l]
+        gw.gathered = None if gat is None else gat[l]
+        gw.gscale = None if gsc is None else gsc[l]
+    group = hs.hs_layer_group_create([gw.pool for gw in gws])
+    tot = np.zeros(3, np.int64)
+    try:
+        for s in range(steps):
+            topk = torch.stack([gw.topk[s] for gw in gws]).contiguous()
+            hs.hs_resolve_topk_layers(group, gws[0].req_ids, topk, res, gat, gsc, cnt)
+            for l, gw in enumerate(gws):
+                err = gw.pool.get_error()
+                out = ots[l].resolve(np.arange(B), gw.topk_host[s], nthreads=nthreads)
+                compare_resolve(gw, ots[l], *out, err, s)
+                tot += out[3].sum(axis=0)
+    finally:
+        hs.hs_layer_group_destroy(group)
+        for gw in gws:
+            gw.pool.close()
+    return tot
+
+
+@pytest.mark.parametrize("name", ["hybrid", "resident", "noresident_small_k"])
+@pytest.mark.parametrize("in_place", [False, True])
+def test_resolve_layers_parity(name, in_place):
+    w = SMALL[name]
+    tot = _run_layers(w, 3, min(w.steps, 4), in_place=in_place)
+    assert tot.sum() > 0
+
+
+def test_layer_group_argument_errors():
+    import tiered_sparse_mla_gb300 as hs
+    from harness import GpuWorkload
+    a = GpuWorkload(W.WORKLOADS["tiny"], build_topk=False)
+    b = GpuWorkload(W.WORKLOADS["tiny"].scaled(hot_rows=1024), build_topk=False)
+    with pytest.raises(hs.HsError) as e:  # pools of different hot-buffer sizes
+        hs.hs_layer_group_create([a.pool, b.pool])
+    assert e.value.status == hs.HS_ERR_INVALID_ARG
+    with pytest.raises(hs.HsError):
+        hs.hs_layer_group_create([])
+    a.pool.close()
+    b.pool.close()

@@ -33,6 +33,7 @@ EXPORTED = [
     "hs_pool_get_error", "hs_resolve_topk", "hs_sparse_mla_decode",
     "hs_decode_workspace_bytes", "hs_status_string", "hs_sparse_mla_decode_static_ws",
     "hs_pool_check_bounded_wait", "hs_resolve_topk_union", "hs_sparse_mla_decode_per_token",
+    "hs_layer_group_create", "hs_layer_group_destroy", "hs_resolve_topk_layers",
 ]
 HS_STATIC_DECODE_WS_BYTES = 24 << 20
 
@@ -96,6 +97,9 @@ def load() -> C.CDLL:
                                             C.c_float, vp, vp, vp], i32),
         "hs_status_string": ([i32], C.c_char_p),
         "hs_resolve_topk_union": ([vp, i32, vp, vp, i32, vp, vp, vp, vp, vp], i32),
+        "hs_layer_group_create": ([C.POINTER(vp), i32, C.POINTER(vp)], i32),
+        "hs_layer_group_destroy": ([vp], i32),
+        "hs_resolve_topk_layers": ([vp, i32, vp, vp, i32, vp, vp, vp, vp, vp], i32),
         "hs_sparse_mla_decode_per_token": ([vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp,
                                             C.c_float, vp, vp, vp, sz, vp], i32),
         "hs_pool_check_bounded_wait": ([vp, C.c_uint32, vp], i32),
@@ -177,6 +181,29 @@ def hs_resolve_topk_union(pool: int, req_ids, topk_idx, resolved, gathered, gath
     K = topk_idx.numel() // max(B, 1)
     _check("hs_resolve_topk_union", load().hs_resolve_topk_union(
         pool, B, _ptr(req_ids), _ptr(topk_idx), K, _ptr(resolved), _ptr(gathered),
+        _ptr(gathered_scale), _ptr(counts), _stream(stream)))
+
+
+def hs_layer_group_create(pools) -> int:
+    """Group of pools (one per layer) for hs_resolve_topk_layers; returns a handle."""
+    arr = (C.c_void_p * len(pools))(*[p.handle if hasattr(p, "handle") else p for p in pools])
+    h = C.c_void_p()
+    _check("hs_layer_group_create", load().hs_layer_group_create(arr, len(pools), C.byref(h)))
+    return h.value
+
+
+def hs_layer_group_destroy(group: int):
+    _check("hs_layer_group_destroy", load().hs_layer_group_destroy(group))
+
+
+def hs_resolve_topk_layers(group: int, req_ids, topk_idx, resolved, gathered, gathered_scale,
+                           counts, stream=None):
+    """All layers' resolve in one launch (see hs.h). topk_idx / resolved int32
+    [L][B][K]; gathered [L][B][K][row_bytes] or None; gathered_scale [L][B][K]
+    or None; counts int32 [L][B][3]."""
+    _, B, K = topk_idx.shape
+    _check("hs_resolve_topk_layers", load().hs_resolve_topk_layers(
+        group, B, _ptr(req_ids), _ptr(topk_idx), K, _ptr(resolved), _ptr(gathered),
         _ptr(gathered_scale), _ptr(counts), _stream(stream)))
 
 

@@ -164,6 +164,7 @@ __device__ __forceinline__ int block_scan_flag(int flag, int *s_warp, int &total
 // Launchers implemented in the .cu files.
 hs_status hs_launch_resolve(hs_pool *pool, int32_t B, const int32_t *req_ids, const int32_t *topk,
                             int32_t K, int32_t *resolved, void *gathered, float *gscale,
-                            int32_t *counts, cudaStream_t stream, int uni);
+                            int32_t *counts, cudaStream_t stream, int uni,
+                            const hs::DevPool *layers, int nlayers);
 size_t hs_resolve_smem_bytes(int K, int G, int C, int RB, bool stage);
 hs_status hs_resolve_prepare(hs_pool *pool);

@@ -40,6 +40,8 @@
 // Barriers are hardware cluster barriers: no spin loops.
 #include <algorithm>
 #include <cstdint>
+#include <new>
+#include <vector>
 
 #include "hs_internal.cuh"
 
@@ -146,7 +148,7 @@ __device__ __forceinline__ void reg_stage(unsigned long long (&x)[8], int t, int
 }
 
 // s: the keys at swz(e), e < n2 (a power of two, 8 <= n2 <= 8 * NT); sorted in place.
-__device__ __noinline__ void sort_keys_reg(unsigned long long *s, int n2, int tid) {
+__device__ __forceinline__ void sort_keys_reg(unsigned long long *s, int n2, int tid) {
     const int T = n2 >> 3;  // threads holding keys
     const bool act = tid < T;
     unsigned long long x[8];
@@ -230,12 +232,15 @@ constexpr size_t kStageSmemCap = 110 * 1024;
 
 // BIG: lists longer than 2048 entries (up to 4096 misses sort in registers).
 // Shorter lists use the kernel without that path, which holds fewer registers.
-template <int RB, bool BIG>
-__global__ void __launch_bounds__(NT, 2)
-resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
-               const int32_t *__restrict__ topk, int K, int chunk, int G,
-               int32_t *__restrict__ resolved, uint8_t *__restrict__ gathered,
-               float *__restrict__ gscale, int32_t *__restrict__ counts, int uni) {
+// PT: the pool as a kernel parameter (hs::DevPool, one layer) or as a
+// reference into device memory (const hs::DevPool &, a layer of a group).
+template <int RB, bool BIG, typename PT>
+__device__ __forceinline__ void resolve_body(PT P, const int32_t *__restrict__ req_ids,
+                                             const int32_t *__restrict__ topk, int K, int chunk,
+                                             int G, int32_t *__restrict__ resolved,
+                                             uint8_t *__restrict__ gathered,
+                                             float *__restrict__ gscale,
+                                             int32_t *__restrict__ counts, int uni) {
     constexpr int V = RB / 16;  // 16-byte vectors per row
     extern __shared__ __align__(16) unsigned char smem[];
     const int W = G - 1;
@@ -688,6 +693,32 @@ resolve_kernel(hs::DevPool P, const int32_t *__restrict__ req_ids,
     if (err) atomicOr(P.err, err);
 }
 
+template <int RB, bool BIG>
+__global__ void __launch_bounds__(NT, 2)
+resolve_kernel(const hs::DevPool P, const int32_t *__restrict__ req_ids,
+               const int32_t *__restrict__ topk, int K, int chunk, int G,
+               int32_t *__restrict__ resolved, uint8_t *__restrict__ gathered,
+               float *__restrict__ gscale, int32_t *__restrict__ counts, int uni) {
+    resolve_body<RB, BIG, hs::DevPool>(P, req_ids, topk, K, chunk, G, resolved, gathered, gscale,
+                                       counts, uni);
+}
+
+// One launch over (request, layer) pairs: layer z = blockIdx.z has its own pool
+// (its table addresses, copied to the device when the layer group was made)
+// and its own slice of every per-entry array.
+template <int RB, bool BIG>
+__global__ void __launch_bounds__(NT, 2)
+resolve_layers_kernel(const hs::DevPool *__restrict__ layers, const int32_t *__restrict__ req_ids,
+               const int32_t *__restrict__ topk, int K, int chunk, int G,
+               int32_t *__restrict__ resolved, uint8_t *__restrict__ gathered,
+               float *__restrict__ gscale, int32_t *__restrict__ counts, int uni) {
+    const size_t ents = (size_t)blockIdx.z * gridDim.y * K;
+    resolve_body<RB, BIG, const hs::DevPool &>(
+        layers[blockIdx.z], req_ids, topk + ents, K, chunk, G, resolved + ents,
+        gathered ? gathered + ents * RB : nullptr, gscale ? gscale + ents : nullptr,
+        counts + (size_t)blockIdx.z * gridDim.y * 3, uni);
+}
+
 int pick_cluster(int K) {
     // one bookkeeping CTA + up to 7 workers (portable cluster size), each
     // worker owning at least 32 entries
@@ -721,18 +752,27 @@ hs_status hs_resolve_prepare(hs_pool *pool) {
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx));
     HS_CUDA_TRY(cudaFuncSetAttribute(resolve_kernel<576, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx));
+    HS_CUDA_TRY(cudaFuncSetAttribute(resolve_layers_kernel<1152, false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx));
+    HS_CUDA_TRY(cudaFuncSetAttribute(resolve_layers_kernel<576, false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx));
+    HS_CUDA_TRY(cudaFuncSetAttribute(resolve_layers_kernel<1152, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx));
+    HS_CUDA_TRY(cudaFuncSetAttribute(resolve_layers_kernel<576, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx));
     return HS_OK;
 }
 
 hs_status hs_launch_resolve(hs_pool *pool, int32_t B, const int32_t *req_ids, const int32_t *topk,
                             int32_t K, int32_t *resolved, void *gathered, float *gscale,
-                            int32_t *counts, cudaStream_t stream, int uni) {
+                            int32_t *counts, cudaStream_t stream, int uni,
+                            const hs::DevPool *layers, int nlayers) {
     const int G = pick_cluster(K);
     const int chunk = (K + G - 2) / (G - 1);
     const size_t smem =
         hs_resolve_smem_bytes(K, G, pool->cfg.hot_rows, pool->row_bytes, gathered == nullptr);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(G, B, 1);
+    cfg.gridDim = dim3(G, B, nlayers);
     cfg.blockDim = dim3(NT, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -743,20 +783,34 @@ hs_status hs_launch_resolve(hs_pool *pool, int32_t B, const int32_t *req_ids, co
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const hs::DevPool P = pool->dev();
     cudaError_t e;
     auto *uc = static_cast<uint8_t *>(gathered);
     const bool big = K > 2048;
-    if (pool->row_bytes == 1152)
-        e = big ? cudaLaunchKernelEx(&cfg, resolve_kernel<1152, true>, P, req_ids, topk, (int)K,
-                                     chunk, G, resolved, uc, gscale, counts, uni)
-                : cudaLaunchKernelEx(&cfg, resolve_kernel<1152, false>, P, req_ids, topk, (int)K,
-                                     chunk, G, resolved, uc, gscale, counts, uni);
-    else
-        e = big ? cudaLaunchKernelEx(&cfg, resolve_kernel<576, true>, P, req_ids, topk, (int)K,
-                                     chunk, G, resolved, uc, gscale, counts, uni)
-                : cudaLaunchKernelEx(&cfg, resolve_kernel<576, false>, P, req_ids, topk, (int)K,
-                                     chunk, G, resolved, uc, gscale, counts, uni);
+    const int Ki = K;
+    if (layers) {
+        if (pool->row_bytes == 1152)
+            e = big ? cudaLaunchKernelEx(&cfg, resolve_layers_kernel<1152, true>, layers, req_ids,
+                                         topk, Ki, chunk, G, resolved, uc, gscale, counts, uni)
+                    : cudaLaunchKernelEx(&cfg, resolve_layers_kernel<1152, false>, layers, req_ids,
+                                         topk, Ki, chunk, G, resolved, uc, gscale, counts, uni);
+        else
+            e = big ? cudaLaunchKernelEx(&cfg, resolve_layers_kernel<576, true>, layers, req_ids,
+                                         topk, Ki, chunk, G, resolved, uc, gscale, counts, uni)
+                    : cudaLaunchKernelEx(&cfg, resolve_layers_kernel<576, false>, layers, req_ids,
+                                         topk, Ki, chunk, G, resolved, uc, gscale, counts, uni);
+    } else {
+        const hs::DevPool P = pool->dev();
+        if (pool->row_bytes == 1152)
+            e = big ? cudaLaunchKernelEx(&cfg, resolve_kernel<1152, true>, P, req_ids, topk, Ki,
+                                         chunk, G, resolved, uc, gscale, counts, uni)
+                    : cudaLaunchKernelEx(&cfg, resolve_kernel<1152, false>, P, req_ids, topk, Ki,
+                                         chunk, G, resolved, uc, gscale, counts, uni);
+        else
+            e = big ? cudaLaunchKernelEx(&cfg, resolve_kernel<576, true>, P, req_ids, topk, Ki,
+                                         chunk, G, resolved, uc, gscale, counts, uni)
+                    : cudaLaunchKernelEx(&cfg, resolve_kernel<576, false>, P, req_ids, topk, Ki,
+                                         chunk, G, resolved, uc, gscale, counts, uni);
+    }
     return e == cudaSuccess ? HS_OK : HS_ERR_CUDA;
 }
 
@@ -778,7 +832,8 @@ hs_status resolve_entry(hs_pool_t pool, int32_t B, const int32_t *d_req_ids,
     if ((reinterpret_cast<uintptr_t>(d_gathered) & 15u) != 0) return HS_ERR_INVALID_ARG;
     if (B == 0) return HS_OK;
     return hs_launch_resolve(pool, B, d_req_ids, d_topk_idx, K, d_resolved, d_gathered,
-                             d_gathered_scale, d_counts, static_cast<cudaStream_t>(stream), uni);
+                             d_gathered_scale, d_counts, static_cast<cudaStream_t>(stream), uni,
+                             nullptr, 1);
 }
 }  // namespace
 
@@ -799,4 +854,76 @@ extern "C" hs_status hs_resolve_topk_union(hs_pool_t pool, int32_t B, const int3
                                            void *stream) {
     return resolve_entry(pool, B, d_req_ids, d_topk_idx, K, d_resolved, d_gathered,
                          d_gathered_scale, d_counts, stream, 1);
+}
+
+// ---------------------------------------------------------------- layer groups
+// The pools of several sparse-MLA layers, resolved in one launch whose grid
+// spans (request, layer) pairs ("vLLM GLM 5.3 优化：混合 HiSparse 卸载", 关键架构细节,
+// 轻量级执行: all sparse-MLA layers launched at once, in stream order).
+struct hs_layer_group {
+    int L = 0;
+    hs_pool *first = nullptr;
+    hs::DevPool *d_pools = nullptr;  // [L] device copies of the pools' table pointers
+};
+
+extern "C" hs_status hs_layer_group_create(const hs_pool_t *pools, int32_t L,
+                                           hs_layer_group_t *out) {
+    if (!pools || !out || L < 1 || L > 65535) return HS_ERR_INVALID_ARG;
+    *out = nullptr;
+    const hs_pool *p0 = pools[0];
+    if (!p0) return HS_ERR_INVALID_ARG;
+    std::vector<hs::DevPool> host(L);
+    for (int l = 0; l < L; ++l) {
+        const hs_pool *p = pools[l];
+        if (!p || p->device != p0->device || p->cfg.dtype != p0->cfg.dtype ||
+            p->cfg.hot_rows != p0->cfg.hot_rows || p->cfg.max_topk != p0->cfg.max_topk)
+            return HS_ERR_INVALID_ARG;
+        host[l] = p->dev();
+    }
+    int cur = 0;
+    HS_CUDA_TRY(cudaGetDevice(&cur));
+    if (cur != p0->device) return HS_ERR_INVALID_ARG;
+    auto *g = new (std::nothrow) hs_layer_group;
+    if (!g) return HS_ERR_OUT_OF_MEMORY;
+    if (cudaMalloc(&g->d_pools, L * sizeof(hs::DevPool)) != cudaSuccess) {
+        delete g;
+        return HS_ERR_OUT_OF_MEMORY;
+    }
+    if (cudaMemcpy(g->d_pools, host.data(), L * sizeof(hs::DevPool), cudaMemcpyHostToDevice) !=
+        cudaSuccess) {
+        cudaFree(g->d_pools);
+        delete g;
+        return HS_ERR_CUDA;
+    }
+    g->L = L;
+    g->first = pools[0];
+    *out = g;
+    return HS_OK;
+}
+
+extern "C" hs_status hs_layer_group_destroy(hs_layer_group_t g) {
+    if (!g) return HS_ERR_INVALID_ARG;
+    cudaFree(g->d_pools);
+    delete g;
+    return HS_OK;
+}
+
+extern "C" hs_status hs_resolve_topk_layers(hs_layer_group_t g, int32_t B, const int32_t *d_req_ids,
+                                            const int32_t *d_topk_idx, int32_t K,
+                                            int32_t *d_resolved, void *d_gathered,
+                                            float *d_gathered_scale, int32_t *d_counts,
+                                            void *stream) {
+    if (!g || B < 0 || !d_req_ids || !d_topk_idx || !d_resolved || !d_counts)
+        return HS_ERR_INVALID_ARG;
+    hs_pool *pool = g->first;
+    if (K < 1 || K > pool->cfg.max_topk || K > pool->cfg.hot_rows) return HS_ERR_CAPACITY;
+    if (B > 65535) return HS_ERR_INVALID_ARG;
+    const bool fp8 = pool->cfg.dtype == HS_FP8_E4M3_ROWSCALE;
+    if (d_gathered ? fp8 != (d_gathered_scale != nullptr) : d_gathered_scale != nullptr)
+        return HS_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(d_gathered) & 15u) != 0) return HS_ERR_INVALID_ARG;
+    if (B == 0) return HS_OK;
+    return hs_launch_resolve(pool, B, d_req_ids, d_topk_idx, K, d_resolved, d_gathered,
+                             d_gathered_scale, d_counts, static_cast<cudaStream_t>(stream), 0,
+                             g->d_pools, g->L);
 }
