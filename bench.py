@@ -180,8 +180,8 @@ DESCS = {
 DEFAULT_STEPS = {"resident": 2000, "tiny": 2000, "hybrid": 512, "noresident": 256, "agent": 715}
 
 
-def _link_peak_gbs():
-    """Measured pinned host -> device copy bandwidth (best of 3, 256 MiB)."""
+def _link_peak_gbs(to_host: bool = False):
+    """Measured pinned host <-> device copy bandwidth (best of 3, 256 MiB)."""
     import torch
     h = torch.empty(256 << 20, dtype=torch.uint8).pin_memory()
     d = torch.empty_like(h, device="cuda")
@@ -189,7 +189,10 @@ def _link_peak_gbs():
     for _ in range(3):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        d.copy_(h, non_blocking=True)
+        if to_host:
+            h.copy_(d, non_blocking=True)
+        else:
+            d.copy_(h, non_blocking=True)
         e1.record()
         torch.cuda.synchronize()
         best = max(best, h.numel() / (e0.elapsed_time(e1) * 1e-3) / 1e9)
@@ -465,6 +468,74 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def run_transitions(args):
+    """Residency transitions on the resident workload's shape: every request
+    fully resident with a host block reserved per page; one active-copy launch
+    copies every finished page to host memory (timed), then one demotion
+    launch releases every request's pages before its last 32K tokens (timed).
+    Prints one JSON line."""
+    import numpy as np
+    import torch
+    import __graft_entry__ as g
+    g.build()
+    import tiered_sparse_mla_gb300 as hs
+    import workloads as W
+    w = W.WORKLOADS[args.workload if args.workload != "agent" else WORKLOAD]
+    if args.batch:
+        w = w.scaled(B=args.batch)
+    P, hb = w.pages, w.hot_rows // 64
+    pool = hs.Pool(dtype=hs.HS_FP8_E4M3_ROWSCALE if w.dtype == "fp8" else hs.HS_BF16,
+                   n_gpu_blocks=w.B * (P + hb), n_host_blocks=w.B * P, max_requests=w.B,
+                   max_ctx=w.ctx, max_topk=w.K, hot_rows=w.hot_rows)
+    page_gpu = np.arange(w.B * P, dtype=np.int32).reshape(w.B, P)
+    for r in range(w.B):
+        pool.request_init(r, w.ctx)
+        pool.page_map_range(r, 0, page_gpu[r], np.full(P, -1, np.int32))
+        pool.hot_lease(r, w.B * P + r * hb + np.arange(hb))
+    W.fill_rows(w.dtype, pool.gpu_rows(), pool.gpu_scales(), W.row_seed(w, "gpu"))
+    reqs = np.repeat(np.arange(w.B), P - 1).astype(np.int32)
+    pages = np.tile(np.arange(P - 1), w.B).astype(np.int32)
+    t_req = torch.from_numpy(reqs).cuda()
+    t_pg = torch.from_numpy(pages).cuda()
+    t_hb = torch.from_numpy(reqs * P + pages).cuda()
+    keep = torch.full((w.B,), 32768, dtype=torch.int32, device="cuda")
+    rq = torch.arange(w.B, dtype=torch.int32, device="cuda")
+    freed = torch.empty((w.B, P), dtype=torch.int32, device="cuda")
+    nfreed = torch.empty(w.B, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    with torch.cuda.stream(stream):
+        hs.hs_active_copy(pool.handle, t_req[:w.B], t_pg[:w.B], t_hb[:w.B], stream)  # warm-up
+        stream.synchronize()
+        ev[0].record(stream)
+        hs.hs_active_copy(pool.handle, t_req, t_pg, t_hb, stream)
+        ev[1].record(stream)
+        hs.hs_demote_cold_pages(pool.handle, rq, keep, freed, nfreed, stream)
+        ev[2].record(stream)
+    torch.cuda.synchronize()
+    assert pool.get_error() == 0
+    copy_ms, demote_ms = ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])
+    n_pages = len(reqs)
+    bytes_ = n_pages * 64 * (w.row_bytes + (4 if w.dtype == "fp8" else 0))
+    gbs = bytes_ / (copy_ms * 1e-3) / 1e9
+    peak = _link_peak_gbs(to_host=True)
+    line = {"metric": "residency transitions: active copy GB/s, demotion time", "impl": "gb300",
+            "value": round(gbs, 1), "unit": "GB/s device-to-host (active copy)",
+            "higher_is_better": True, "n_gpus": 1, "data": "synthetic",
+            "config": {"workload": f"{DESCS.get(w.name, w.name)} [batch {w.B}]",
+                       "pages_copied": n_pages, "bytes_copied": bytes_,
+                       "demotion": "every request keeps its last 32768 tokens"},
+            "active_copy_ms": round(copy_ms, 3), "demote_ms": round(demote_ms, 4),
+            "pages_freed": int(nfreed.sum().item()),
+            "roofline": {"bound": "host-link", "achieved": round(gbs, 1), "peak": round(peak, 1),
+                         "unit": "GB/s", "frac": round(gbs / peak, 4),
+                         "peak_source": "measured live: pinned 256 MiB device-to-host copy"},
+            "gpu_launches": 2}
+    print(json.dumps(line), flush=True)
+    pool.close()
+
+
 def run_e2e(args, gw, qs, stream, w):
     """Same step through the C ABI, inputs copied from pinned host memory and the
     result (out, lse) read back to host memory inside the timed region.
@@ -662,6 +733,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="requests per step (default: the workload's; smaller only for profiling)")
+    ap.add_argument("--transitions", action="store_true",
+                    help="time the active copy and the demotion kernels (one JSON line)")
     ap.add_argument("--layers", type=int, default=1,
                     help="L layers (own pools and lists): one multi-layer resolve launch per step")
     ap.add_argument("--per-token", action="store_true",
@@ -678,6 +751,8 @@ def main():
     args.steps = args.steps or DEFAULT_STEPS[args.workload]
     if args.impl == "reference":
         run_reference(args)
+    elif args.transitions:
+        run_transitions(args)
     else:
         run_gpu(args)
 

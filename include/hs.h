@@ -55,6 +55,8 @@ typedef enum {
 #define HS_DEVERR_BAD_REQUEST 8u  /* request id outside [0, max_requests)         */
 #define HS_DEVERR_CAPACITY    16u /* more misses than unprotected hot slots       */
 #define HS_DEVERR_TIMEOUT     32u /* a bounded device wait gave up                */
+#define HS_DEVERR_BAD_PAGE    64u /* a page transition named a page, block or tail
+                                     it cannot apply to (that entry is skipped)     */
 
 typedef enum { HS_BF16 = 0, HS_FP8_E4M3_ROWSCALE = 1 } hs_kv_dtype;
 
@@ -267,6 +269,35 @@ hs_status hs_sparse_mla_decode_static_ws(hs_pool_t pool, int32_t B, int32_t T, i
                                          const float *d_gathered_scale, const int32_t *d_resolved,
                                          const int32_t *d_topk_idx, const int32_t *d_req_ids,
                                          float sm_scale, void *d_out, float *d_lse, void *stream);
+
+/* ---- residency transitions on the device -------------------------------- */
+
+/* Active copy ([A] 混合 HiSparse 的技术实现 item 1; 关键架构细节, 主动复制): for each
+ * of n triples (d_req[i], d_page[i], d_host_block[i]) the page's 64 rows (and
+ * FP8 scales) are copied from its GPU block into that block of the pinned host
+ * arena, then the page table records the host copy; the page stays resident
+ * and keeps being served from the GPU. One launch, asynchronous on `stream`;
+ * it touches only the host half of page-table entries, which the resolve reads
+ * for non-resident pages only, so it may run on a side stream next to the
+ * decode path. A triple whose request, page or host block is out of range, or
+ * whose page has no GPU block, is skipped and sets HS_DEVERR_BAD_PAGE. The
+ * caller owns host-block allocation. */
+hs_status hs_active_copy(hs_pool_t pool, int32_t n, const int32_t *d_req, const int32_t *d_page,
+                         const int32_t *d_host_block, void *stream);
+
+/* Demotion under pressure ([A] 混合 HiSparse 的技术实现 item 2; [B] 分级内存的运作机制):
+ * request d_req[i] keeps its last d_keep_tail[i] tokens on the GPU and releases
+ * its coldest pages, read as its oldest: every page p with (p+1)*64 <=
+ * ctx_len - keep_tail that is resident and has a host copy loses its GPU
+ * block. Pages without a host copy stay resident. The freed GPU blocks go to
+ * d_freed[i][0 .. d_n_freed[i]) in ascending page order (d_freed is
+ * [n][max_pages] int32, d_n_freed [n] int32) for the caller's allocator. One
+ * launch, asynchronous on `stream`; order it with the resolve calls of the
+ * same requests. A bad request id sets HS_DEVERR_BAD_REQUEST, a negative tail
+ * HS_DEVERR_BAD_PAGE (that request frees nothing). */
+hs_status hs_demote_cold_pages(hs_pool_t pool, int32_t n, const int32_t *d_req,
+                               const int32_t *d_keep_tail, int32_t *d_freed, int32_t *d_n_freed,
+                               void *stream);
 
 /* Failure-detection check: launches one device wait on a barrier phase that
  * nothing completes, bounded by limit_us (1 .. 2,000,000) exactly like the

@@ -32,6 +32,7 @@ ERR_DUPLICATE = 2
 ERR_NO_HOST = 4
 ERR_BAD_REQUEST = 8
 ERR_CAPACITY = 16
+ERR_BAD_PAGE = 64
 
 PAGE = 64
 
@@ -144,6 +145,56 @@ class OracleTiers:
                       _p(self.tag), _p(self.stamp), _p(self.pos_to_slot), _p(self.clock),
                       _p(self.ctx_len), _p(self.pool_rows), _p(self.pool_scales),
                       _p(self.host_rows), _p(self.host_scales))
+
+    # ------------------------------------------------------------ residency transitions
+    def active_copy(self, reqs, pages, host_blocks) -> int:
+        """Active copy ("vLLM GLM 5.3 优化：混合 HiSparse 卸载", 混合 HiSparse 的技术实现
+        item 1 and 关键架构细节, 主动复制): a finished page of a resident request is
+        copied to host memory while the GPU keeps serving it. For each triple
+        (r, p, hb), in order: the 64 rows (and scales) of the page's GPU block
+        are copied into host block hb, and the page table records hb as the
+        page's host copy. A triple with r, p or hb out of range, or whose page
+        has no GPU block, changes nothing and sets ERR_BAD_PAGE. Needs a
+        writable host arena of the oracle's own. Returns the error bits."""
+        R, P = self.page_gpu.shape
+        n_hb = self.host_rows.shape[0] // PAGE
+        err = 0
+        for r, p, hb in zip(np.asarray(reqs).tolist(), np.asarray(pages).tolist(),
+                            np.asarray(host_blocks).tolist()):
+            if not (0 <= r < R and 0 <= p < P and 0 <= hb < n_hb) or self.page_gpu[r, p] < 0:
+                err |= ERR_BAD_PAGE
+                continue
+            gb = int(self.page_gpu[r, p])
+            self.host_rows[hb * PAGE:(hb + 1) * PAGE] = self.pool_rows[gb * PAGE:(gb + 1) * PAGE]
+            if self.fp8:
+                self.host_scales[hb * PAGE:(hb + 1) * PAGE] = self.pool_scales[gb * PAGE:(gb + 1) * PAGE]
+            self.page_host[r, p] = hb
+        return err
+
+    def demote(self, reqs, keep_tail):
+        """Demotion under pressure (same page, 混合 HiSparse 的技术实现 item 2; "vLLM
+        Hybrid HiSparse：稀疏MLA破解长上下文显存瓶颈", 分级内存的运作机制): a request
+        keeps its tail on the GPU and releases its coldest pages, read as its
+        oldest: every page p with (p+1)*64 <= ctx_len - keep_tail that is
+        resident and has a host copy loses its GPU block. Returns (per request
+        the freed GPU blocks in ascending page order, error bits); a bad request
+        id (ERR_BAD_REQUEST) or a negative tail (ERR_BAD_PAGE) frees nothing."""
+        R, P = self.page_gpu.shape
+        freed, err = [], 0
+        for r, kt in zip(np.asarray(reqs).tolist(), np.asarray(keep_tail).tolist()):
+            out = []
+            if not 0 <= r < R:
+                err |= ERR_BAD_REQUEST
+            elif kt < 0:
+                err |= ERR_BAD_PAGE
+            else:
+                ncold = min(max(0, (int(self.ctx_len[r]) - kt) // PAGE), P)
+                for p in range(ncold):
+                    if self.page_gpu[r, p] >= 0 and self.page_host[r, p] >= 0:
+                        out.append(int(self.page_gpu[r, p]))
+                        self.page_gpu[r, p] = -1
+            freed.append(np.array(out, np.int32))
+        return freed, err
 
     def reset_request(self, r: int):
         self.tag[r] = -1

@@ -23,6 +23,7 @@ HS_OK, HS_ERR_INVALID_ARG, HS_ERR_CAPACITY, HS_ERR_OUT_OF_MEMORY = 0, 1, 2, 3
 HS_ERR_CUDA, HS_ERR_DEVICE_DATA, HS_ERR_TIMEOUT, HS_ERR_UNSUPPORTED = 4, 5, 6, 7
 HS_DEVERR_INDEX_RANGE, HS_DEVERR_DUPLICATE, HS_DEVERR_NO_HOST = 1, 2, 4
 HS_DEVERR_BAD_REQUEST, HS_DEVERR_CAPACITY, HS_DEVERR_TIMEOUT = 8, 16, 32
+HS_DEVERR_BAD_PAGE = 64
 HS_BF16, HS_FP8_E4M3_ROWSCALE = 0, 1
 
 EXPORTED = [
@@ -34,6 +35,7 @@ EXPORTED = [
     "hs_decode_workspace_bytes", "hs_status_string", "hs_sparse_mla_decode_static_ws",
     "hs_pool_check_bounded_wait", "hs_resolve_topk_union", "hs_sparse_mla_decode_per_token",
     "hs_layer_group_create", "hs_layer_group_destroy", "hs_resolve_topk_layers",
+    "hs_active_copy", "hs_demote_cold_pages",
 ]
 HS_STATIC_DECODE_WS_BYTES = 24 << 20
 
@@ -100,6 +102,8 @@ def load() -> C.CDLL:
         "hs_layer_group_create": ([C.POINTER(vp), i32, C.POINTER(vp)], i32),
         "hs_layer_group_destroy": ([vp], i32),
         "hs_resolve_topk_layers": ([vp, i32, vp, vp, i32, vp, vp, vp, vp, vp], i32),
+        "hs_active_copy": ([vp, i32, vp, vp, vp, vp], i32),
+        "hs_demote_cold_pages": ([vp, i32, vp, vp, vp, vp, vp], i32),
         "hs_sparse_mla_decode_per_token": ([vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp,
                                             C.c_float, vp, vp, vp, sz, vp], i32),
         "hs_pool_check_bounded_wait": ([vp, C.c_uint32, vp], i32),
@@ -205,6 +209,20 @@ def hs_resolve_topk_layers(group: int, req_ids, topk_idx, resolved, gathered, ga
     _check("hs_resolve_topk_layers", load().hs_resolve_topk_layers(
         group, B, _ptr(req_ids), _ptr(topk_idx), K, _ptr(resolved), _ptr(gathered),
         _ptr(gathered_scale), _ptr(counts), _stream(stream)))
+
+
+def hs_active_copy(pool: int, req, page, host_block, stream=None):
+    """Active copy of pages to host blocks (see hs.h); int32 device tensors [n]."""
+    _check("hs_active_copy", load().hs_active_copy(
+        pool, req.numel(), _ptr(req), _ptr(page), _ptr(host_block), _stream(stream)))
+
+
+def hs_demote_cold_pages(pool: int, req, keep_tail, freed, n_freed, stream=None):
+    """Demotion of each request's pages before its tail (see hs.h). req, keep_tail,
+    n_freed int32 [n]; freed int32 [n][max_pages]."""
+    _check("hs_demote_cold_pages", load().hs_demote_cold_pages(
+        pool, req.numel(), _ptr(req), _ptr(keep_tail), _ptr(freed), _ptr(n_freed),
+        _stream(stream)))
 
 
 def hs_decode_workspace_bytes(B: int, T: int, H: int, K: int) -> int:
