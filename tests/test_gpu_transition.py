@@ -84,12 +84,12 @@ def test_active_copy_demote_then_resolve(dtype):
     assert f.pool.get_error() == 0
     assert f.ot.active_copy(reqs, pages, hbs) == 0
     f.check_tables()
-    host = f.pool.host_rows()
-    n = (reqs.max() + 1) * w.pages * PAGE
-    assert np.array_equal(host[:n], f.ot.host_rows[:n])
+    # the copied host blocks (the others hold whatever the arena held before)
+    rows = (hbs[:, None] * PAGE + np.arange(PAGE)).reshape(-1)
+    assert np.array_equal(f.pool.host_rows()[rows], f.ot.host_rows[rows])
     if dtype == "fp8":
-        assert np.array_equal(f.pool.host_scales()[:n].view(np.uint32),
-                              f.ot.host_scales[:n].view(np.uint32))
+        assert np.array_equal(f.pool.host_scales()[rows].view(np.uint32),
+                              f.ot.host_scales[rows].view(np.uint32))
     # demotion: request 0 to the workload's tail, 1 to nothing, 2 keeps everything
     keep = np.array([w.resident_tail, 0, w.ctx], np.int32)
     freed = torch.full((w.B, w.pages), -7, dtype=torch.int32, device="cuda")

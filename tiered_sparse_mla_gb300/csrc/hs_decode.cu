@@ -115,6 +115,15 @@ struct Cfg {
     static_assert(SMEM_ALLOC <= 232448, "shared memory");
 };
 
+// Programmatic dependent launch: this grid may start while the previous kernel
+// on the stream (the step's resolve) is still running; a thread waits here for
+// that kernel's completion and memory before reading anything it wrote.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel on the stream (the split merge) be scheduled early.
+__device__ __forceinline__ void grid_dep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 struct DecParams {
     const int32_t *resolved, *topk, *req_ids, *ctx;
     const float *gscale;        // gathered row scales (FP8, gathered rows)
@@ -361,6 +370,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     tc_fence_after();
     cluster_sync_all();  // the peer's barriers are initialised before any remote arrive
     const uint32_t tmem = static_cast<uint32_t>(misc[0]);
+    grid_dep_launch();
+    // the producer first issues the Q loads (Q does not come from the resolve)
+    if (warp != 0) grid_dep_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -373,6 +385,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 tma_load_3d(sQst + c * QCH_BYTES, &tm_q, 64 * (5 * half + c), mt * BM, b,
                             bar(C::B_QFULL));
         }
+        grid_dep_wait();
         constexpr uint32_t ROWB = FP8 ? 64u : 128u;  // smem bytes of one row of one chunk
         // in place: pool row ids of this lane's four rows, loaded a tile ahead
         auto row_ids = [&](int i, int (&rid)[4]) {
@@ -834,6 +847,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 __global__ void __launch_bounds__(256)
 combine_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_lse, int nsplit,
                int rows, __nv_bfloat16 *__restrict__ out, float *__restrict__ lse) {
+    grid_dep_wait();  // the decode grid's partials are complete
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -967,13 +981,16 @@ hs_status launch_decode(dim3 grid, cudaStream_t s, const CUtensorMap &tq, const 
     cfg.blockDim = dim3(NTHR, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_ALLOC;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;  // the two output halves of one work unit
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // may start before the previous kernel ends (it waits in griddepcontrol.wait)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, decode_tc_kernel<FP8, INPLACE>, tq, tk, p) == cudaSuccess
                ? HS_OK
                : HS_ERR_CUDA;
@@ -1070,8 +1087,18 @@ hs_status decode_entry(hs_pool_t pool, int32_t B, int32_t T, int32_t tpl, int32_
     if (st != HS_OK) return st;
     if (pl.nsplit > 1) {
         const int rows = B * pl.M;
-        combine_kernel<<<(rows + 7) / 8, 256, 0, s>>>(p.ws_o, p.ws_lse, pl.nsplit, rows, p.out, d_lse);
-        if (cudaGetLastError() != cudaSuccess) return HS_ERR_CUDA;
+        cudaLaunchConfig_t cc = {};
+        cc.gridDim = dim3((rows + 7) / 8, 1, 1);
+        cc.blockDim = dim3(256, 1, 1);
+        cc.stream = s;
+        cudaLaunchAttribute ca[1];
+        ca[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        ca[0].val.programmaticStreamSerializationAllowed = 1;
+        cc.attrs = ca;
+        cc.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cc, combine_kernel, (const float *)p.ws_o, (const float *)p.ws_lse,
+                               pl.nsplit, rows, p.out, d_lse) != cudaSuccess)
+            return HS_ERR_CUDA;
     }
     return HS_OK;
 }

@@ -242,6 +242,9 @@ __device__ __forceinline__ void resolve_body(PT P, const int32_t *__restrict__ r
                                              float *__restrict__ gscale,
                                              int32_t *__restrict__ counts, int uni) {
     constexpr int V = RB / 16;  // 16-byte vectors per row
+    // the step's decode may be scheduled as soon as every CTA of this grid runs
+    // (it waits for this grid to complete before reading what it wrote)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ __align__(16) unsigned char smem[];
     const int W = G - 1;
     const Smem L{chunk, max(8, next_pow2(K)), K, P.C};
