@@ -131,7 +131,8 @@ struct DecParams {
     const uint8_t *gathered;
     int zero_row;               // pool row of zeros read for absent entries (in place)
     __nv_bfloat16 *out;
-    float *lse, *ws_o, *ws_lse;
+    float *lse, *ws_lse;
+    __half *ws_o;  // split partials, f16 (normalised O of one split, |O| ~ |V|)
     uint32_t *err;
     int B, T, H, K, M, nsplit, kps, max_req, row_bytes;
     int tpl;  // lists per request: list b is token b % tpl of request b / tpl
@@ -815,14 +816,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
                         }
                     } else {
-                        float4 *dst = reinterpret_cast<float4 *>(
+                        uint4 *dst = reinterpret_cast<uint4 *>(
                             p.ws_o + (((size_t)split * p.B + b) * p.M + mg) * 512 + col);
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            dst[q] = make_float4(__uint_as_float(o[4 * q]) * inv,
-                                                 __uint_as_float(o[4 * q + 1]) * inv,
-                                                 __uint_as_float(o[4 * q + 2]) * inv,
-                                                 __uint_as_float(o[4 * q + 3]) * inv);
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                w[e] = pack2<true>(__uint_as_float(o[8 * q + 2 * e]) * inv,
+                                                   __uint_as_float(o[8 * q + 2 * e + 1]) * inv);
+                            dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
                     }
                 }
             }
@@ -845,7 +849,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
 // Merges the KV-split partials: out = sum_s w_s O_s / sum_s w_s, w_s = exp(lse_s - max).
 __global__ void __launch_bounds__(256)
-combine_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_lse, int nsplit,
+combine_kernel(const __half *__restrict__ ws_o, const float *__restrict__ ws_lse, int nsplit,
                int rows, __nv_bfloat16 *__restrict__ out, float *__restrict__ lse) {
     grid_dep_wait();  // the decode grid's partials are complete
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -863,14 +867,16 @@ combine_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_lse,
             if (ls == -INFINITY) continue;
             const float w = __expf(ls - mx);
             wsum += w;
-            const float4 *src = reinterpret_cast<const float4 *>(ws_o + ((size_t)s * rows + row) * 512);
+            const uint2 *src = reinterpret_cast<const uint2 *>(ws_o + ((size_t)s * rows + row) * 512);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const float4 v = src[lane + 32 * q];
-                acc[4 * q] += w * v.x;
-                acc[4 * q + 1] += w * v.y;
-                acc[4 * q + 2] += w * v.z;
-                acc[4 * q + 3] += w * v.w;
+                const uint2 u = src[lane + 32 * q];  // elements 4 (lane + 32 q) .. + 3
+                const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
+                const float2 c = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
+                acc[4 * q] += w * a.x;
+                acc[4 * q + 1] += w * a.y;
+                acc[4 * q + 2] += w * c.x;
+                acc[4 * q + 3] += w * c.y;
             }
         }
     }
@@ -917,7 +923,7 @@ Plan make_plan(int B, int T, int H, int K) {
     pl.nsplit = (K + pl.kps - 1) / pl.kps;
     if (pl.nsplit > 1) {
         const size_t rows = (size_t)pl.nsplit * B * pl.M;
-        pl.ws_o_bytes = (rows * 512 * sizeof(float) + 255) & ~size_t(255);
+        pl.ws_o_bytes = (rows * 512 * sizeof(__half) + 255) & ~size_t(255);
         pl.ws_bytes = pl.ws_o_bytes + ((rows * sizeof(float) + 255) & ~size_t(255));
     }
     return pl;
@@ -1063,7 +1069,7 @@ hs_status decode_entry(hs_pool_t pool, int32_t B, int32_t T, int32_t tpl, int32_
     p.row_bytes = fp8 ? hs::kDim : 2 * hs::kDim;
     p.out = static_cast<__nv_bfloat16 *>(d_out);
     p.lse = d_lse;
-    p.ws_o = pl.nsplit > 1 ? static_cast<float *>(d_workspace) : nullptr;
+    p.ws_o = pl.nsplit > 1 ? static_cast<__half *>(d_workspace) : nullptr;
     p.ws_lse = pl.nsplit > 1
                    ? reinterpret_cast<float *>(static_cast<uint8_t *>(d_workspace) + pl.ws_o_bytes)
                    : nullptr;
@@ -1096,7 +1102,7 @@ hs_status decode_entry(hs_pool_t pool, int32_t B, int32_t T, int32_t tpl, int32_
         ca[0].val.programmaticStreamSerializationAllowed = 1;
         cc.attrs = ca;
         cc.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cc, combine_kernel, (const float *)p.ws_o, (const float *)p.ws_lse,
+        if (cudaLaunchKernelEx(&cc, combine_kernel, (const __half *)p.ws_o, (const float *)p.ws_lse,
                                pl.nsplit, rows, p.out, d_lse) != cudaSuccess)
             return HS_ERR_CUDA;
     }
