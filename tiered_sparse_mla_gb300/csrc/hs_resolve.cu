@@ -362,7 +362,9 @@ __device__ __forceinline__ void resolve_body(PT P, const int32_t *__restrict__ r
                     }
                 }
             }
-            const bool miss = (kind & 15) == KIND_MISS;
+            // a union sends rank 0 one key per distinct position (its reader's);
+            // the other occurrences take the reader's slot after barrier B
+            const bool miss = (kind & 15) == KIND_MISS && (!uni || s_claim[l] == j0 + l);
             const unsigned bal = __ballot_sync(0xffffffffu, miss);
             if (bal) {
                 const int leader = __ffs(bal) - 1;
@@ -464,6 +466,24 @@ __device__ __forceinline__ void resolve_body(PT P, const int32_t *__restrict__ r
         hs::cluster_wait();    // barrier A (long complete)
         hs::cluster_arrive();  // barrier B
         hs::cluster_wait();    // barrier B: rank 0 has placed every miss
+
+        if (uni) {
+            // occurrences that did not read their row: the reader's slot row,
+            // from the reader's owner (-2 - row, as repeats are encoded; -1
+            // when the position was rejected); each placed one counts as a miss
+            int placed = 0;
+            for (int mi = tid; mi < nm; mi += NT) {
+                const int l = s_mj[mi];
+                const int cj = s_claim[l];
+                if (cj == j0 + l) continue;
+                const int owner = 1 + cj / chunk;
+                const int d = hs::dsmem_ld(hs::dsmem_map(&s_src[cj - (owner - 1) * chunk], owner));
+                s_src[l] = d >= 0 ? -2 - d : -1;
+                placed += d >= 0;
+            }
+            if (placed) atomicAdd(&counts[bi * 3 + 2], placed);
+            __syncthreads();
+        }
 
         // ------------------------------------------------------------ phase 3
         // Each placed position's row goes into its hot slot once, written by
