@@ -386,8 +386,9 @@ __device__ __forceinline__ void resolve_body(PT P, const int32_t *__restrict__ r
         __syncthreads();
         // this worker's totals into rank 0 (one writer per slot)
         if (tid < 3) hs::dsmem_st(hs::dsmem_map(&s_wcnt[4 * g + tid], 0), s_misc[tid]);
-        __threadfence();  // hot-hit stamps visible to rank 0 before barrier A
         __syncthreads();
+        // the arrive releases (cluster scope) the hot-hit stamps, the keys and
+        // the totals to rank 0, which acquires them in its wait
         hs::cluster_arrive();  // barrier A
 
         // ------------------------------------------------------------ phase 2
@@ -708,9 +709,8 @@ __device__ __forceinline__ void resolve_body(PT P, const int32_t *__restrict__ r
             counts[bi * 3 + 1] = tot_hot;
             counts[bi * 3 + 2] = served;
         }
-        __threadfence();
         __syncthreads();
-        hs::cluster_arrive();  // barrier B: miss slots published
+        hs::cluster_arrive();  // barrier B: miss slots (and counts) released to the workers
         hs::cluster_wait();
     }
     if (err) atomicOr(P.err, err);
