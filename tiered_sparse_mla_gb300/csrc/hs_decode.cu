@@ -446,13 +446,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             constexpr uint32_t ID_PV = idesc_f16(FP8 ? 0u : 1u, 1, BM, 256);
             bool ok = mbar_wait(bar(C::B_QREADY), 0);
             tc_fence_after();
-            // Order QK_0, QK_1, QK_2, then PV_i, QK_{i+3}: the softmax threads
-            // release P_i at about the time the stagers, two tiles ahead, free
-            // S_{i+2}, so each wait is short and suspends instead of spinning.
-            for (int i = -3; i < ntiles && ok; ++i) {
-                if (i >= 0) {
-                    ok = mbar_wait(bar(C::B_PFULL), (uint32_t)i & 1u) && !misc[1];
-                    if (!ok) break;
+            // PV_i as soon as P_i is ready (it frees tile group i % NG for the
+            // next load); otherwise QK_j once tile j has landed and the stagers
+            // have read S_{j-1}. Each test is on the next phase of its barrier
+            // (the previous one has completed, or the MMA that needs it would
+            // not have been issued), so a parity test cannot see a stale phase.
+            // An idle spell longer than 2 s gives up like every other wait.
+            int i = 0, j = 0;
+            uint64_t idle0 = 0;
+            while (ok && i < ntiles) {
+                if (misc[1]) {
+                    ok = false;
+                    break;
+                }
+                if (j > i && mbar_test(bar(C::B_PFULL), (uint32_t)i & 1u)) {
                     // O[128 x 256] += P_i[128 x 64] V_i[64 x 256]; frees tile group i % NG
                     tc_fence_after();
                     const uint64_t vb = desc_sw128(slot(i % NG, 0), KCH_BYTES, 1024);
@@ -466,13 +473,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         mma_ts<true>(tmem + TM_O, tmem + TM_P + 8u * kk, lo + 128u * kk, hi, ID_PV);
                     mma_commit(bar(C::B_GEMPTY + i % NG));
                     mma_commit(bar(C::B_PVDONE));
+                    ++i;
+                    idle0 = 0;
+                    continue;
                 }
-                const int j = i + 3;
-                if (j < ntiles) {
-                    // tile j landed and S_{j-1} read by the stagers
-                    ok = mbar_wait(bar(C::B_GFULL + j % NG), (uint32_t)(j / NG) & 1u) &&
-                         (j == 0 || mbar_wait(bar(C::B_SFREE), (uint32_t)(j - 1) & 1u)) && !misc[1];
-                    if (!ok) break;
+                if (j < ntiles && mbar_test(bar(C::B_GFULL + j % NG), (uint32_t)(j / NG) & 1u) &&
+                    (j == 0 || mbar_test(bar(C::B_SFREE), (uint32_t)(j - 1) & 1u))) {
                     tc_fence_after();
                     const uint64_t b0 = desc_sw128(slot(j % NG, lc0), 16, 1024);
                     if (half)
@@ -480,7 +486,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     else
                         issue_qk<5>(tmem + TM_S, tmem + TM_Q, (uint32_t)b0, (uint32_t)(b0 >> 32), ID_QK);
                     mma_commit(bar(C::B_SFULL));
+                    ++j;
+                    idle0 = 0;
+                    continue;
                 }
+                const uint64_t now = globaltimer();
+                if (!idle0)
+                    idle0 = now;
+                else if (now - idle0 > 2000000000ull)
+                    ok = false;
+                __nanosleep(32);
             }
             if (!ok) fail();
             // every MMA issued above has finished before TMEM and smem are released
