@@ -12,7 +12,11 @@ Pins (tests marked ``not gpu``): hand-computed LRU scenarios under
 ``tests/golden/``, two independent formulations of the LRU rule checked
 against each other, the state invariants, brute-force dense MLA attention in
 float64 via ``torch`` on small inputs, closed-form special cases, and all 256
-e4m3 codes against ``torch.float8_e4m3fn``.
+e4m3 codes against ``torch.float8_e4m3fn``. The union of per-token lists is
+pinned to the single-list rule with repeats blanked; per-token attention to
+the shared-list MTP decode; the residency transitions (plain numpy here) to
+the workloads' tail layout, to invariants, and to the resolve serving demoted
+rows with their original bytes.
 """
 from __future__ import annotations
 
