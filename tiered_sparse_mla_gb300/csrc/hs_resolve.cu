@@ -18,25 +18,30 @@
 // repeat of a missing position resolves to the row its first occurrence took;
 // only the first occurrence updates the LRU state and copies the row.
 //
-// Design (GB300): one thread-block cluster of G CTAs per request. Rank 0 keeps
-// the request's LRU bookkeeping; ranks 1..G-1 ("workers") own K/(G-1) list
-// entries each.
+// Design (GB300): one thread-block cluster of G CTAs per request (and layer,
+// when a launch covers several layers' pools). Rank 0 keeps the request's LRU
+// bookkeeping; ranks 1..G-1 ("workers") own K/(G-1) list entries each.
 //   start    cluster barrier (every CTA's shared memory is live);
 //   phase 1  workers classify their entries (page table, then pos_to_slot),
 //            stamp their hot hits, and push each miss's (position, list index)
-//            key straight into rank 0's shared memory; -> cluster barrier A
-//   rank 0   sorts the keys (bitonic, in shared memory), ranks distinct
-//            positions, stages the persistent LRU order (slots kept sorted by
-//            (stamp, slot), so the i-th unprotected entry is the i-th victim)
-//            in shared memory, places the misses (tag / stamp / pos_to_slot /
-//            LRU order) and writes each miss's slot into its owner's shared
-//            memory;
+//            key into rank 0's key array (slots taken by one remote atomic per
+//            warp). In a union the first occurrence to mark pos_to_slot is the
+//            position's reader and the only one to push a key; -> barrier A
+//   rank 0   sorts the keys (bitonic, shared memory or registers), ranks the
+//            distinct positions, stages the persistent LRU order (slots kept
+//            sorted by (stamp, slot), so the i-th unprotected entry is the
+//            i-th victim) in shared memory, places the misses (tag / stamp /
+//            pos_to_slot / LRU order) and writes each miss's slot into its
+//            owner's shared memory;
 //   phase 2  meanwhile workers copy every row whose gathered position is known
-//            -- resident and hot rows from the pool, miss rows from the
-//            device-mapped pinned host arena -- into the gathered buffer, so
-//            the host-link reads overlap rank 0's bookkeeping; -> barrier B
-//   phase 3  workers copy each placed miss row from the gathered buffer into
-//            its hot slot (HBM to HBM) and zero rejected ones.
+//            -- resident and hot rows from the pool, miss rows they read from
+//            the device-mapped pinned host arena -- into the gathered buffer
+//            (rows kept in the pool: the miss rows into shared memory), so the
+//            host-link reads overlap rank 0's bookkeeping; -> barrier B
+//   phase 3  a union's other occurrences take their reader's slot (through
+//            distributed shared memory; -> barrier C before any CTA exits);
+//            readers copy each placed miss row into its hot slot and rejected
+//            entries get zeros.
 // Barriers are hardware cluster barriers: no spin loops.
 #include <algorithm>
 #include <cstdint>
