@@ -10,7 +10,10 @@
  * of ordinary blocks leased from that same pool, and pinned host memory.
  * hs_resolve_topk makes every selected row GPU-addressable in one fused,
  * CUDA-graph-capturable launch; hs_sparse_mla_decode then runs MLA attention
- * over only those K rows.
+ * over only those K rows. Variants: one list per speculative query token
+ * (hs_resolve_topk_union, hs_sparse_mla_decode_per_token), several layers'
+ * pools resolved in one launch (hs_resolve_topk_layers), and the residency
+ * transitions around the path (hs_active_copy, hs_demote_cold_pages).
  *
  * Conventions
  *  - Streams are cudaStream_t values passed as void* (NULL = legacy stream).
