@@ -354,3 +354,47 @@ def test_union_of_token_lists_on_workload(oracle_lib):
             assert len(np.unique(tags)) == len(tags)
             assert np.array_equal(gat[b], ot.pool_rows[res[b]])
             assert np.array_equal(gsc[b].view(np.uint32), ot.pool_scales[res[b]].view(np.uint32))
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_union_with_more_distinct_misses_than_slots(oracle_lib, seed):
+    """A union longer than the hot buffer whose distinct missing positions
+    outnumber the free slots: the positions beyond the capacity are rejected
+    with every one of their occurrences (none takes another position's row),
+    exactly as the single-list rule rejects them once repeats are blanked."""
+    rng = np.random.default_rng(3000 + seed)
+    n_pages = int(rng.integers(2, 5))
+    ctx = n_pages * PAGE
+    C = int(rng.integers(2, 10))
+    K = int(rng.integers(C + 1, 3 * C + 1))
+    page_gpu = np.full(n_pages, -1, np.int32)
+    page_host = np.arange(n_pages, dtype=np.int32)   # every row misses unless hot
+    hot_block = n_pages
+    mk = lambda: _tiers(oracle_lib, page_gpu[None], page_host[None], np.array([[hot_block]]),
+                        ctx, C, 16, 64 * (n_pages + 1), 64 * n_pages,
+                        np.random.default_rng(seed), max_ctx=ctx)
+    u, d = mk(), mk()
+    universe = rng.choice(ctx, size=min(ctx, 2 * K), replace=False)
+    rejected_seen = 0
+    for step in range(8):
+        topk = rng.choice(universe, size=K, replace=True).astype(np.int32)
+        first, rep = {}, np.zeros(K, bool)
+        for j, p in enumerate(topk.tolist()):
+            if p in first:
+                rep[j] = True
+            else:
+                first[p] = j
+        blank = topk.copy()
+        blank[rep] = -1
+        ru, _, _, cu, eu = u.resolve([0], topk[None], union=True)
+        rd, _, _, cd, ed = d.resolve([0], blank[None])
+        want = rd[0].copy()
+        for j in np.nonzero(rep)[0]:
+            want[j] = rd[0][first[int(topk[j])]]
+        assert np.array_equal(ru[0], want)
+        assert eu == ed and not (eu & 2)
+        assert cu.sum() == cd.sum() + int((want[rep] >= 0).sum())
+        rejected_seen += int((want < 0).sum())
+        for a, b in ((u.tag, d.tag), (u.stamp, d.stamp), (u.pos_to_slot, d.pos_to_slot)):
+            assert np.array_equal(a, b)
+    assert rejected_seen > 0  # the case does overflow
