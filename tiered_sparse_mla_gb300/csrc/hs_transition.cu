@@ -114,7 +114,6 @@ extern "C" hs_status hs_active_copy(hs_pool_t pool, int32_t n, const int32_t *d_
         return HS_ERR_INVALID_ARG;
     if (pool->cfg.n_host_blocks < 1) return HS_ERR_INVALID_ARG;
     if (n == 0) return HS_OK;
-    if (n > 2147483647) return HS_ERR_INVALID_ARG;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int hb = static_cast<int>(pool->cfg.n_host_blocks);
     float *hsc = pool->hd_scales;
