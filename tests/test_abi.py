@@ -46,3 +46,30 @@ def test_product_path_does_not_touch_the_oracle():
     for rel in ("tiered_sparse_mla_gb300/__init__.py", "harness.py", "workloads/__init__.py"):
         text = open(os.path.join(ROOT, rel)).read()
         assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), rel
+
+
+def test_entry_points_reject_null_handles_without_a_device():
+    """Host-side checks come first: every hot-path and transition entry point
+    returns HS_ERR_INVALID_ARG for a NULL pool or group, touching no device."""
+    import ctypes as C
+    import tiered_sparse_mla_gb300 as hs
+    lib = hs.load()
+    buf = (C.c_int32 * 64)()
+    p = C.cast(buf, C.c_void_p)
+    inval = hs.HS_ERR_INVALID_ARG
+    assert lib.hs_resolve_topk(None, 1, p, p, 8, p, None, None, p, None) == inval
+    assert lib.hs_resolve_topk_union(None, 1, p, p, 8, p, None, None, p, None) == inval
+    assert lib.hs_sparse_mla_decode(None, 1, 1, 16, 8, p, p, None, p, p, p, C.c_float(0.1), p, p,
+                                    None, 0, None) == inval
+    assert lib.hs_sparse_mla_decode_per_token(None, 1, 2, 16, 8, p, p, None, p, p, p,
+                                              C.c_float(0.1), p, p, None, 0, None) == inval
+    assert lib.hs_sparse_mla_decode_per_token(None, 1, 0, 16, 8, p, p, None, p, p, p,
+                                              C.c_float(0.1), p, p, None, 0, None) == inval
+    out = C.c_void_p()
+    assert lib.hs_layer_group_create(None, 2, C.byref(out)) == inval
+    arr = (C.c_void_p * 1)(None)
+    assert lib.hs_layer_group_create(arr, 1, C.byref(out)) == inval and out.value is None
+    assert lib.hs_layer_group_destroy(None) == inval
+    assert lib.hs_resolve_topk_layers(None, 1, p, p, 8, p, None, None, p, None) == inval
+    assert lib.hs_active_copy(None, 1, p, p, p, None) == inval
+    assert lib.hs_demote_cold_pages(None, 1, p, p, p, p, None) == inval
