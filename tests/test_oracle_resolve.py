@@ -398,3 +398,37 @@ def test_union_with_more_distinct_misses_than_slots(oracle_lib, seed):
         for a, b in ((u.tag, d.tag), (u.stamp, d.stamp), (u.pos_to_slot, d.pos_to_slot)):
             assert np.array_equal(a, b)
     assert rejected_seen > 0  # the case does overflow
+
+
+def _golden_union():
+    with open(os.path.join(HERE, "golden", "union_cases.json")) as f:
+        return json.load(f)["cases"]
+
+
+@pytest.mark.parametrize("formulation", [0, 1])
+@pytest.mark.parametrize("case", _golden_union(), ids=lambda c: c["name"])
+def test_golden_union(oracle_lib, case, formulation):
+    """Hand-computed unions of per-token lists (tests/golden/union_cases.json)."""
+    rng = np.random.default_rng(6)
+    n_pages = len(case["page_gpu"])
+    n_gpu_rows = 64 * (1 + max(max(case["page_gpu"]), max(case["hot_blocks"])))
+    ot = _tiers(oracle_lib, np.array([case["page_gpu"]]), np.array([case["page_host"]]),
+                np.array([case["hot_blocks"]]), case["ctx_len"], case["hot_rows"], 32,
+                n_gpu_rows, 64 * n_pages, rng, max_ctx=64 * n_pages)
+    host0 = ot.host_rows.copy()
+    for st in case["steps"]:
+        topk = np.array([st["topk"]], np.int32)
+        res, gat, _, cnt, err = ot.resolve([0], topk, formulation=formulation, union=True)
+        assert res[0].tolist() == st["resolved"], st["note"]
+        assert cnt[0].tolist() == st["counts"], st["note"]
+        assert err == st["err"], st["note"]
+        assert ot.tag[0].tolist() == st["tag"], st["note"]
+        assert ot.stamp[0].tolist() == st["stamp"], st["note"]
+        for j, p in enumerate(st["topk"]):
+            r = st["resolved"][j]
+            if r < 0:
+                assert not gat[0, j].any()
+            elif case["page_gpu"][p // PAGE] >= 0:
+                assert np.array_equal(gat[0, j], ot.pool_rows[r])
+            else:
+                assert np.array_equal(gat[0, j], host0[case["page_host"][p // PAGE] * PAGE + p % PAGE])
