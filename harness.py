@@ -76,16 +76,17 @@ class GpuWorkload:
             self.pool.resolve_topk(self.req_ids, t, self.resolved, self.gathered, self.gscale,
                                    self.counts, stream)
 
-    def decode(self, step: int, q, topk=None, stream=None):
+    def decode(self, step: int, q, topk=None, stream=None, sm_scale=None):
         t = self.topk[step] if topk is None else topk
+        sc = self.w.sm_scale if sm_scale is None else sm_scale
         if self.per_token:
             self.pool.sparse_mla_decode_per_token(q, self.gathered, self.gscale, self.resolved,
-                                                  t, self.req_ids, self.w.sm_scale, self.out,
-                                                  self.lse, self.workspace, stream)
+                                                  t, self.req_ids, sc, self.out, self.lse,
+                                                  self.workspace, stream)
         else:
             self.pool.sparse_mla_decode(q, self.gathered, self.gscale, self.resolved, t,
-                                        self.req_ids, self.w.sm_scale, self.out, self.lse,
-                                        self.workspace, stream)
+                                        self.req_ids, sc, self.out, self.lse, self.workspace,
+                                        stream)
 
 
 class GpuAgent:

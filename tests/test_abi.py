@@ -73,3 +73,29 @@ def test_entry_points_reject_null_handles_without_a_device():
     assert lib.hs_resolve_topk_layers(None, 1, p, p, 8, p, None, None, p, None) == inval
     assert lib.hs_active_copy(None, 1, p, p, p, None) == inval
     assert lib.hs_demote_cold_pages(None, 1, p, p, p, p, None) == inval
+
+
+def test_static_workspace_entry_point_host_checks():
+    """The allocation-free decode rejects a NULL pool before touching a device,
+    and every workload shape of the benchmark fits its fixed array: with the
+    split rule (splits x requests x M tiles x 2 <= SM count) the f16/bf16
+    partials stay under 64 KB per SM, far below the array's size."""
+    import ctypes as C
+    import tiered_sparse_mla_gb300 as hs
+    import workloads as W
+    lib = hs.load()
+    buf = (C.c_int32 * 64)()
+    p = C.cast(buf, C.c_void_p)
+    assert lib.hs_sparse_mla_decode_static_ws(None, 1, 1, 16, 8, p, p, None, p, p, p,
+                                              C.c_float(0.1), p, p, None) == hs.HS_ERR_INVALID_ARG
+    shapes = [(w.B, w.T, w.H, w.K) for w in W.WORKLOADS.values()]
+    a = W.AgentMix()
+    shapes.append((a.B, a.T, a.H, a.K))
+    shapes += [(w.B * w.T, 1, w.H, w.K) for w in W.WORKLOADS.values()]  # one list per token
+    for B in (1, 2, 3, 5, 8, 13, 16, 32, 64, 128):
+        for T in (1, 2, 4):
+            for H in (16, 64, 128):
+                shapes.append((B, T, H, 2048))
+    for B, T, H, K in shapes:
+        need = lib.hs_decode_workspace_bytes(B, T, H, K)
+        assert need <= hs.HS_STATIC_DECODE_WS_BYTES, (B, T, H, K, need)

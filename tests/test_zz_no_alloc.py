@@ -4,7 +4,9 @@ For callers that cannot allocate device memory (an engine that has reserved
 the device's memory for its own KV pool, a C plugin without an allocator), the
 library offers decode with its split-KV scratch in a fixed array inside the
 library. Called through the C ABI, twice in a row, it must give what the
-allocating entry point gives, within the tolerances the decode tests use.
+allocating entry point gives. Both run the same kernels with the same split
+of the keys on the same inputs, so the outputs must agree bit for bit (a
+wrong offset into the fixed array would show up here).
 This file sorts last so that a run stopping at the first failure has run every
 other test first; it also passes when run alone.
 """
@@ -17,9 +19,6 @@ import torch
 import workloads as W
 
 pytestmark = pytest.mark.gpu
-
-TOL = {"bf16": 2e-2, "fp8": 5e-2}
-LSE_TOL = 1e-2
 
 
 @pytest.mark.parametrize("name", ["resident", "hybrid"])
@@ -39,7 +38,7 @@ def test_static_workspace_decode_matches_allocating_entry_point(name):
     gw.resolve(0)
     gw.decode(0, q)  # allocating entry point, caller-provided workspace
     torch.cuda.synchronize()
-    ref_out, ref_lse = gw.out.float().clone(), gw.lse.clone()
+    ref_out, ref_lse = gw.out.clone(), gw.lse.clone()
 
     lib = hs.load()
     stream = torch.cuda.current_stream().cuda_stream
@@ -53,11 +52,7 @@ def test_static_workspace_decode_matches_allocating_entry_point(name):
             out.data_ptr(), lse.data_ptr(), stream)
         assert st == hs.HS_OK, hs.status_string(st)
         torch.cuda.synchronize()
-        o = out.float()
-        rel = ((o - ref_out).norm(dim=-1) / ref_out.norm(dim=-1).clamp_min(1e-6)).max().item()
-        assert rel <= TOL[w.dtype], f"call {call}: rel err {rel:.3e}"
-        fin = torch.isfinite(ref_lse)
-        assert torch.equal(fin, torch.isfinite(lse))
-        assert (lse[fin] - ref_lse[fin]).abs().max().item() <= LSE_TOL
+        assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16)), f"call {call}: out"
+        assert torch.equal(lse.view(torch.int32), ref_lse.view(torch.int32)), f"call {call}: lse"
     assert gw.pool.get_error() == 0
     gw.pool.close()

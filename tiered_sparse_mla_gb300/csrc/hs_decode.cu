@@ -1,4 +1,4 @@
-// hs_decode.cu -- sparse MLA decode over the gathered top-K latent rows, on
+// hs_decode.cu -- sparse MLA decode over the selected top-K latent rows, on
 // tcgen05 tensor cores (sm_103a).
 //
 // Attention restricted to the K rows the indexer selected ("vLLM GLM 5.3 优化：
@@ -12,49 +12,47 @@
 // dense contractions: S[128 x 64] = Q[128 x 576] K^T, O[128 x 512] = P V.
 //
 // Work unit: (request, 128-row M tile, KV split), run by a cluster of two CTAs.
-// The 576-wide rows are nine 64-column chunks. CTA h (h = 0, 1):
-//   - holds Q for its share of the QK depth (chunks 0-4 for h = 0, 5-8 for
-//     h = 1) in tensor memory and accumulates O for output columns
-//     [256h, 256h + 256) (V chunks 0-3 or 4-7); per 64-key tile it therefore
-//     loads only chunks 4h..4h+4;
-//   - computes a partial S over its depth share into TMEM, sends it (rounded
-//     to f16 after scaling by sm_scale * log2 e) to the peer through
-//     distributed shared memory and adds the peer's partial; both CTAs add
-//     the same two rounded values, so they hold bit-identical S and take
-//     identical softmax decisions;
-//   - runs O_h += P V_h on its own V chunks, with P in tensor memory.
-// Four tile groups are in flight, and a tile's partial S leaves for the peer
-// two tiles before its softmax, so the exchange overlaps the softmax of the
-// tile in between.
-// Roles inside a CTA (384 threads):
-//   warp 0     TMA producer: Q once, into the space of tile groups 2-3 (their
-//              first loads wait until Q has moved to TMEM), then one 5-chunk
-//              tile group per 64 keys (no L2 prefetch: with four groups in
-//              flight per CTA the loads already keep HBM busy, and a
-//              prefetch only queues ahead of them in the same copy engine);
-//   warp 1     MMA issuer (one thread): S_j = Q K_j^T into the TMEM S buffer
-//              (A = Q from TMEM) once tile j has landed and S_{j-1} has been
-//              read; O += P_i V_i (A = P from TMEM, V read from the same smem
-//              chunks as K through an MN-major descriptor, no transpose
-//              stored) once P_i is written;
-//   warp 2     per tile: the lowest query token that sees each key (from the
-//              resolved flags, top-K positions and context length) into a
-//              shared ring, so that no softmax warp waits on a global load;
-//              FP8 only: convert e4m3 chunks in place to f16 with the row
-//              scale folded in;
-//   warp 3     courier: sends each staged partial to the peer in one bulk
-//              shared-to-shared copy;
-//   warps 4-7  stagers, one thread per query row (TMEM lane): read S, free it
-//              for the next QK, and write the partial as f16 of
-//              S * sm_scale * log2(e) for the courier;
-//   warps 8-11 softmax, one thread per query row: add the two partials
-//              (then one thread tells the peer its partial has been read),
-//              masking (skipped for tiles every row sees), online softmax
-//              with a conditional rescale (the running max only moves when a
-//              tile's max exceeds it by 2^8), P to TMEM, epilogue.
-// Stagers run up to two tiles ahead of the softmax, so the exchange of a
-// tile's partials overlaps the softmax of the tiles before it.
-// TMEM (512 columns): O half 256 | S 64 | P 32 | Q 160.
+// The 576-wide rows are nine 64-column chunks: eight value chunks and the rope
+// chunk 8. CTA h (h = 0, 1):
+//   - loads, per 64-key tile, its four value chunks 4h..4h+3 and the rope
+//     chunk (40 KB of BF16 rows, 20 KB of FP8 codes);
+//   - holds Q in tensor memory for those value chunks and for its half of the
+//     rope chunk (columns 32h..32h+31 of it), so that each CTA computes S over
+//     288 of the 576 depth columns;
+//   - sends its partial S, in f32 and already multiplied by sm_scale*log2(e)
+//     (times the row scale for FP8), straight from registers to the peer's
+//     shared memory (each warp's stores, then one release-arrive per warp on
+//     the peer's barrier) and adds the peer's partial; f32 addition is
+//     commutative, so both CTAs hold bit-identical S and take identical
+//     softmax decisions;
+//   - accumulates O for output columns [256h, 256h + 256) (its value chunks)
+//     with P in tensor memory.
+// FP8 rows: the codes are turned into BF16 exactly (each code's bits placed as
+// a BF16 of value code * 2^-120, then multiplied by 2^120); the row's fp32
+// scale multiplies the scores of that key in f32, and its probability before
+// P is rounded to BF16 (the sum of probabilities stays unscaled). So Q stays
+// BF16 on both paths and no operand is rounded beyond BF16.
+// Roles inside a CTA (256 threads for BF16 rows, 384 for FP8):
+//   warp 0      TMA producer: Q once, into the space of tile groups 2-3 (their
+//               first loads wait until Q has moved to TMEM), then per tile one
+//               box of the four value chunks and one of the rope chunk (or, in
+//               place, four-row gathers from the pool);
+//   warp 1      MMA issuer (one thread): S_j = Q K_j^T into the TMEM S buffer
+//               once tile j is ready and S_{j-1} has been read; O += P_i V_i
+//               (V read from the same smem chunks as K through an MN-major
+//               descriptor) once P_i is written; PV first when both can go;
+//   warp 2      per tile: the lowest query token that sees each key, and for
+//               FP8 the key's row scale, into shared rings, so that no row
+//               thread waits on a global load;
+//   warp 3      idle;
+//   warps 4-7   row threads, one per query row (TMEM lane): read S_{j+1},
+//               free it for the next QK and send the partial to the peer, then
+//               the softmax of tile j (add the peer's partial, mask, online
+//               softmax with a conditional rescale, P to TMEM), epilogue. The
+//               send of tile j+1 goes out before the softmax of tile j, so the
+//               exchange overlaps the softmax;
+//   warps 8-11  FP8 only: convert each landed tile of codes to BF16 in place.
+// TMEM (512 columns): O half 256 | S 64 | P 32 | Q 144.
 // Every mbarrier wait is bounded in time; on expiry the kernel sets
 // HS_DEVERR_TIMEOUT, drains its own copies and MMAs and returns. Roles hand
 // over through mbarriers only, so one that gives up leaves no other waiting
@@ -64,8 +62,10 @@
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <climits>
 #include <cstdint>
+#include <mutex>
 
 #include "hs_internal.cuh"
 #include "hs_tc.cuh"
@@ -74,44 +74,55 @@ namespace {
 
 using namespace hs::tc;
 
-constexpr int NTHR = 384;  // 12 warps
-constexpr int NSTG = 128;  // stager threads (warps 4-7)
-constexpr int NSFT = 128;  // softmax threads (warps 8-11)
+constexpr int NSTG = 128;            // stager threads (warps 4-7)
+constexpr int NSFT = 128;            // softmax threads (warps 8-11)
+constexpr int NCVT = NSTG;           // FP8: the stagers also convert the codes
 constexpr int BM = 128, BN = 64;
-constexpr int NLC = 5;               // chunks a CTA loads per 64-key tile
+constexpr int NLC = 5;               // chunks a CTA loads per 64-key tile: 4 value + rope
 constexpr int NG = 4;                // tile groups in flight
-constexpr int NQ_MAX = 5;            // Q chunks a CTA holds
+constexpr int NQC = 5;               // Q chunks staged per CTA (4 value + rope)
 constexpr int QCH_BYTES = BM * 128;  // 128 rows x 64 columns x 2 B
 constexpr int KCH_BYTES = BN * 128;  // 64 keys x 64 columns x 2 B
 constexpr int FCH_BYTES = BN * 64;   // 64 keys x 64 e4m3 codes
-constexpr int X_BYTES = BM * 128;    // 128 rows x 64 f16 partial scores
+constexpr int GRP_BYTES = NLC * KCH_BYTES;
+constexpr int CVT_UNITS = NLC * FCH_BYTES / 16 / NCVT;  // 16-byte code units per converter per tile
+constexpr int X_BYTES = BM * 32 * 4; // 128 rows x 32 f32 partial scores (half a tile)
 constexpr float TAU2 = 8.f;          // rescale threshold, log2 units
 constexpr uint32_t TMEM_COLS = 512, TM_O = 0, TM_S = 256, TM_P = 320, TM_Q = 352;
-static_assert(TM_Q + 32 * NQ_MAX <= TMEM_COLS, "tensor memory");
+static_assert(TM_Q + 4 * 32 + 16 <= TMEM_COLS, "tensor memory");
+
+template <bool FP8>
+struct Threads {
+    static constexpr int N = 384;
+};
 
 struct Cfg {
     static constexpr int OFF_RING = 0;
-    static constexpr int OFF_QSTAGE = OFF_RING + 2 * NLC * KCH_BYTES;  // tile groups 2-3
-    static constexpr int OFF_XIN = OFF_RING + NG * NLC * KCH_BYTES;   // [2] the peer's partial S
+    static constexpr int OFF_QSTAGE = OFF_RING + 2 * GRP_BYTES;       // tile groups 2-3
+    static constexpr int OFF_XIN = OFF_RING + NG * GRP_BYTES;         // [2] the peer's partial S
     static constexpr int OFF_XOUT = OFF_XIN + 2 * X_BYTES;            // [2] own partial S
     static constexpr int OFF_KVIS = OFF_XOUT + 2 * X_BYTES;           // int16 [NG][64]
-    static constexpr int OFF_TDMAX = OFF_KVIS + NG * BN * 2;          // int32 [NG]
-    static constexpr int OFF_BAR = OFF_TDMAX + NG * 4;
+    static constexpr int OFF_KSC = OFF_KVIS + NG * BN * 2;            // f32 [NG][64] FP8 row scales
+    static constexpr int OFF_TDMAX = OFF_KSC + NG * BN * 4;           // int32 [NG][2]
+    static constexpr int OFF_BAR = OFF_TDMAX + NG * 8;
     static constexpr int B_QFULL = 0, B_QREADY = 1, B_DRAIN = 2, B_GFULL = 3;
     static constexpr int B_GEMPTY = B_GFULL + NG, B_GLANDED = B_GEMPTY + NG;
     static constexpr int B_SFULL = B_GLANDED + NG, B_SFREE = B_SFULL + 1;
-    static constexpr int B_PFULL = B_SFREE + 1, B_PVDONE = B_PFULL + 1;
-    static constexpr int B_XFULL = B_PVDONE + 1;    // [2] the peer's partial has landed
+    static constexpr int B_PFULL = B_SFREE + 1;     // [2] P of a half tile (columns 16h..) written
+    static constexpr int B_PVDONE = B_PFULL + 2;    // [2] PV of a half tile done
+    static constexpr int B_XFULL = B_PVDONE + 2;    // [2] the peer's partial has landed
     static constexpr int B_XTAKEN = B_XFULL + 2;    // [2] the peer has read what this CTA sent
     static constexpr int B_STAGED = B_XTAKEN + 2;   // [2] own partial written, ready to send
-    static constexpr int B_READ = B_STAGED + 2;     // [2] both partials of a tile have been read here
-    static constexpr int B_KVIS = B_READ + 2;       // [NG] key visibility of a tile written
+    static constexpr int B_READ = B_STAGED + 2;     // [2] both partials of a half tile read here
+    static constexpr int B_XOUTDONE = B_READ + 2;   // [2] the courier's copy has read X_out
+    static constexpr int B_KVIS = B_XOUTDONE + 2;   // [NG] key visibility (and scales) of a tile
     static constexpr int NBAR = B_KVIS + NG;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // [0] TMEM base, [1] abort flag
     static constexpr int SMEM = OFF_MISC + 16;
     static constexpr int SMEM_ALLOC = SMEM + 1024;       // room to align the base to 1 KiB
-    static_assert(OFF_QSTAGE % 1024 == 0, "swizzled tiles need 1 KiB alignment");
-    static_assert(NQ_MAX * QCH_BYTES <= (NG - 2) * NLC * KCH_BYTES, "Q staging space");
+    static_assert(OFF_QSTAGE % 1024 == 0 && OFF_XIN % 1024 == 0 && OFF_XOUT % 1024 == 0,
+                  "alignment");
+    static_assert(NQC * QCH_BYTES <= (NG - 2) * GRP_BYTES, "Q staging space");
     static_assert(SMEM_ALLOC <= 232448, "shared memory");
 };
 
@@ -128,13 +139,12 @@ struct DecParams {
     const int32_t *resolved, *topk, *req_ids, *ctx;
     const float *gscale;        // gathered row scales (FP8, gathered rows)
     const float *pool_scales;   // pool row scales (FP8, rows read in place)
-    const uint8_t *gathered;
     int zero_row;               // pool row of zeros read for absent entries (in place)
     __nv_bfloat16 *out;
     float *lse, *ws_lse;
-    __half *ws_o;  // split partials, f16 (normalised O of one split, |O| ~ |V|)
+    __nv_bfloat16 *ws_o;  // split partials: normalised O of one split (a weighted mean of value rows)
     uint32_t *err;
-    int B, T, H, K, M, nsplit, kps, max_req, row_bytes;
+    int B, T, H, K, M, nsplit, kps, max_req;
     int tpl;  // lists per request: list b is token b % tpl of request b / tpl
     float scale_log2;
 };
@@ -152,7 +162,14 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t a) {
                  : "memory");
     return v;
 }
-
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t a) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(a)
+                 : "memory");
+    return v;
+}
 // TMEM load of 32 columns whose registers only become valid after the wait;
 // the wait takes them as operands so no use can be scheduled before it.
 #define HS_TMEM_LD32(taddr, r)                                                                    \
@@ -175,7 +192,7 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t a) {
                    "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),  \
                    "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),  \
                    "+r"(r[30]), "+r"(r[31])::"memory")
-// TMEM store of 32 columns of 32-bit words from this thread's lane.
+// TMEM store of 32 (16) columns of 32-bit words from this thread's lane.
 #define HS_TMEM_ST32(taddr, r)                                                                    \
     asm volatile(                                                                                 \
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"   \
@@ -186,7 +203,6 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t a) {
         "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),      \
         "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])                               \
         : "memory")
-
 #define HS_TMEM_ST16(taddr, r)                                                                    \
     asm volatile(                                                                                 \
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"   \
@@ -205,6 +221,15 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int 
         : "memory");
 }
 
+// Shared memory to a box of a 3-D tensor map (bulk async group of this thread).
+__device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(tmap)),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
 // Four rows (r0..r3) of a 2-D tensor map, each one box wide starting at
 // column x, to consecutive box-sized places at dst.
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int x, int r0, int r1,
@@ -216,48 +241,27 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int 
         : "memory");
 }
 
-template <bool FP8>
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-    if (FP8) {
-        __half2 h = __floats2half2_rn(lo, hi);
-        return *reinterpret_cast<uint32_t *>(&h);
-    } else {
-        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-        return *reinterpret_cast<uint32_t *>(&h);
-    }
-}
-
-// (float(a.lo) + float(b.lo), float(a.hi) + float(b.hi)) for two f16 pairs.
-// The sum is symmetric in a and b, bit for bit (a -0 that the first add
-// turns into +0 leaves every sum unchanged).
-__device__ __forceinline__ float2 add_f16x2_f32(uint32_t a, uint32_t b) {
-    float2 r;
-    asm("{\n .reg .b16 al, ah, bl, bh;\n .reg .f32 t0, t1;\n"
-        " mov.b32 {al, ah}, %2;\n mov.b32 {bl, bh}, %3;\n"
-        " add.rn.f32.f16 t0, al, 0f00000000;\n add.rn.f32.f16 t1, ah, 0f00000000;\n"
-        " add.rn.f32.f16 %0, bl, t0;\n add.rn.f32.f16 %1, bh, t1;\n}"
-        : "=f"(r.x), "=f"(r.y)
-        : "r"(a), "r"(b));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-    uint32_t r;
-    const uint16_t v = static_cast<uint16_t>(two_codes);
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, __half2 s) {
-    __half2 h = *reinterpret_cast<__half2 *>(&a);
-    h = __hmul2(h, s);
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
-    const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
-    __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&h);
+// Four e4m3 codes (the bytes of w, lowest first) to four BF16 values, exactly.
+// A code's sign, four exponent bits and three mantissa bits, placed at the
+// BF16 sign, the low four exponent bits and the top three mantissa bits, form
+// a BF16 whose value is the code's times 2^-120: a normal code 2^(e-7)(1+m/8)
+// becomes 2^(e-127)(1+m/8), a subnormal code 2^-6 (m/8) the BF16 subnormal
+// 2^-126 (m/8). Multiplying by 2^120 (exact) gives the code's value.
+__device__ __forceinline__ void e4m3x4_to_bf16(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t t0 = __byte_perm(w, 0u, 0x1404);  // bytes (c1, 0, c0, 0), high to low
+    const uint32_t t1 = __byte_perm(w, 0u, 0x3424);  // bytes (c3, 0, c2, 0)
+    uint32_t a = (t0 & 0x80008000u) | ((t0 >> 4) & 0x07F007F0u);
+    uint32_t b = (t1 & 0x80008000u) | ((t1 >> 4) & 0x07F007F0u);
+    const uint32_t two120 = 0x7B807B80u;  // (2^120, 2^120) in BF16
+    asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(a) : "r"(two120));
+    asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(b) : "r"(two120));
+    lo = a;
+    hi = b;
 }
 
 // One kind::f16 MMA with A from TMEM; the B descriptor comes as two 32-bit
@@ -280,14 +284,14 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint32_t blo, uin
             : "memory");
 }
 
-// S = Q K^T over NC chunks of the depth: A = Q chunk c at TMEM columns
-// aq + 32 c, B = K chunk c at smem descriptor (blo, bhi) + c * chunk bytes.
-// Straight-line: 4 K steps of 16 per chunk.
-template <int NC>
+// S = Q K^T over this CTA's 288 depth columns: the four value chunks (A = Q
+// chunk c at TMEM columns aq + 32 c, B = local chunk c) and its half of the
+// rope chunk (A at aq + 128, B = K steps 2h, 2h + 1 of local chunk 4).
+// Straight-line: 18 MMAs of K = 16.
 __device__ __forceinline__ void issue_qk(uint32_t dS, uint32_t aq, uint32_t blo, uint32_t bhi,
-                                         uint32_t idesc) {
+                                         uint32_t idesc, int half) {
 #pragma unroll
-    for (int c = 0; c < NC; ++c)
+    for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const uint32_t a = aq + 32u * c + 8u * k;
@@ -297,17 +301,21 @@ __device__ __forceinline__ void issue_qk(uint32_t dS, uint32_t aq, uint32_t blo,
             else
                 mma_ts<true>(dS, a, lo, bhi, idesc);
         }
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+        mma_ts<true>(dS, aq + 128u + 8u * k,
+                     blo + (uint32_t)((4 * KCH_BYTES + 32 * (2 * half + k)) >> 4), bhi, idesc);
 }
 
 // Row r, 16-byte chunk c of a 128-byte-per-row tile with the 128-byte swizzle
-// (the TMA layout of Q, and the layout of the S exchange buffers).
+// (the TMA layout of Q and K).
 __device__ __forceinline__ uint32_t x_off(int r, int c) {
     return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
-
 template <bool FP8, bool INPLACE>
-__global__ void __launch_bounds__(NTHR, 1)
-decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+__global__ void __launch_bounds__(Threads<FP8>::N, 1)
+decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
+                 const __grid_constant__ CUtensorMap tm_kr, const __grid_constant__ CUtensorMap tm_o,
                  const DecParams p) {
     using C = Cfg;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -320,18 +328,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int split = blockIdx.x >> 1, mt = blockIdx.y, b = blockIdx.z;
     const int k0 = split * p.kps, k1 = min(p.K, k0 + p.kps);
     const int ntiles = (k1 - k0 + BN - 1) / BN;
-    const int nq = half ? 4 : 5;      // Q chunks held (global chunks 5h .. 5h+nq-1)
-    const int lc0 = half ? 1 : 0;     // first local chunk used by QK (local chunk lc = global 4h+lc)
+    const int nunits = 2 * ntiles;  // half tiles of 32 keys: the exchange and softmax unit
     volatile int32_t *misc = reinterpret_cast<volatile int32_t *>(smem + C::OFF_MISC);
-    int16_t *kvis = reinterpret_cast<int16_t *>(smem + C::OFF_KVIS);
-    volatile int32_t *tdmax = reinterpret_cast<volatile int32_t *>(smem + C::OFF_TDMAX);
     const uint32_t sR = base + C::OFF_RING, sQst = base + C::OFF_QSTAGE;
     const uint32_t sXin = base + C::OFF_XIN, sXout = base + C::OFF_XOUT;
+    const uint32_t sKvis = base + C::OFF_KVIS, sKsc = base + C::OFF_KSC;
+    volatile int32_t *tdmax = reinterpret_cast<volatile int32_t *>(smem + C::OFF_TDMAX);
     auto bar = [&](int i) { return base + C::OFF_BAR + 8u * (uint32_t)i; };
-    auto slot = [&](int g, int lc) { return sR + (uint32_t)((g * NLC + lc) * KCH_BYTES); };
-    // FP8: the e4m3 codes of chunk lc, packed in the upper half of the tile group
+    auto slot = [&](int g, int lc) { return sR + (uint32_t)(g * GRP_BYTES + lc * KCH_BYTES); };
+    // FP8: the e4m3 codes of local chunk lc, packed in the upper half of the tile group
     auto codes = [&](int g, int lc) {
-        return sR + (uint32_t)(g * NLC * KCH_BYTES + NLC * FCH_BYTES + lc * FCH_BYTES);
+        return sR + (uint32_t)(g * GRP_BYTES + NLC * FCH_BYTES + lc * FCH_BYTES);
     };
     auto fail = [&]() {
         misc[1] = 1;
@@ -343,20 +350,21 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         mbar_init(bar(C::B_QREADY), NSTG + NSFT);
         mbar_init(bar(C::B_DRAIN), 1);
         for (int g = 0; g < NG; ++g) {
-            mbar_init(bar(C::B_GFULL + g), FP8 ? 32 : 1);
+            mbar_init(bar(C::B_GFULL + g), FP8 ? NCVT : 1);
             mbar_init(bar(C::B_GEMPTY + g), 1);
             mbar_init(bar(C::B_GLANDED + g), 1);
             mbar_init(bar(C::B_KVIS + g), 32);
         }
         mbar_init(bar(C::B_SFULL), 1);
         mbar_init(bar(C::B_SFREE), NSTG);
-        mbar_init(bar(C::B_PFULL), NSFT);
-        mbar_init(bar(C::B_PVDONE), 1);
         for (int x = 0; x < 2; ++x) {
+            mbar_init(bar(C::B_PFULL + x), NSFT);
+            mbar_init(bar(C::B_PVDONE + x), 1);
             mbar_init(bar(C::B_XFULL + x), 1);  // own arm + the peer's bulk copy bytes
             mbar_init(bar(C::B_XTAKEN + x), 1);
             mbar_init(bar(C::B_STAGED + x), NSTG);
             mbar_init(bar(C::B_READ + x), 1);
+            mbar_init(bar(C::B_XOUTDONE + x), 1);
         }
         misc[1] = 0;
         fence_mbar_init();
@@ -364,7 +372,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (warp == 1) tmem_alloc(base + C::OFF_MISC, TMEM_COLS);
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tm_q);
-        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_kv);
+        prefetch_tmap(&tm_kr);
+        prefetch_tmap(&tm_o);
     }
     tc_fence_before();
     __syncthreads();
@@ -378,12 +388,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         // Lane 0 loads Q and takes each slot; a tile read from the gathered
-        // buffer is one box per chunk (lane 0), a tile read in place from the
-        // pool is 16 four-row gathers per chunk, one per lane 0..15.
+        // buffer is two boxes (lane 0), a tile read in place from the pool is
+        // 16 four-row gathers per chunk, one per lane 0..15.
         if (lane == 0) {
-            mbar_expect_tx(bar(C::B_QFULL), nq * QCH_BYTES);
-            for (int c = 0; c < nq; ++c)
-                tma_load_3d(sQst + c * QCH_BYTES, &tm_q, 64 * (5 * half + c), mt * BM, b,
+            mbar_expect_tx(bar(C::B_QFULL), NQC * QCH_BYTES);
+            for (int c = 0; c < NQC; ++c)
+                tma_load_3d(sQst + c * QCH_BYTES, &tm_q, 64 * (c < 4 ? 4 * half + c : 8), mt * BM, b,
                             bar(C::B_QFULL));
         }
         grid_dep_wait();
@@ -421,14 +431,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 for (int q = 0; q < 4; ++q) rid[q] = rid_next[q] >= 0 ? rid_next[q] : p.zero_row;
                 row_ids(i + 1, rid_next);
                 if (lane == 0) mbar_expect_tx(done, NLC * (FP8 ? FCH_BYTES : KCH_BYTES));
+                __syncwarp();
                 if (lane < 16)
                     for (int lc = 0; lc < NLC; ++lc)
-                        tma_gather4((FP8 ? codes(g, lc) : slot(g, lc)) + 4u * ROWB * lane,
-                                    &tm_k, 64 * (4 * half + lc), rid[0], rid[1], rid[2], rid[3], done);
+                        tma_gather4((FP8 ? codes(g, lc) : slot(g, lc)) + 4u * ROWB * lane, &tm_kv,
+                                    64 * (lc < 4 ? 4 * half + lc : 8), rid[0], rid[1], rid[2], rid[3],
+                                    done);
             } else if (lane == 0) {
-                // all five chunks of the tile's 64 rows in one box: [chunk][row][64]
+                // the four value chunks of the tile's 64 rows in one box
+                // ([chunk][row][64]), the rope chunk in another
                 mbar_expect_tx(done, NLC * (FP8 ? FCH_BYTES : KCH_BYTES));
-                tma_load_4d(FP8 ? codes(g, 0) : slot(g, 0), &tm_k, 0, k0 + i * BN, 4 * half, b, done);
+                tma_load_4d(FP8 ? codes(g, 0) : slot(g, 0), &tm_kv, 0, k0 + i * BN, 4 * half, b, done);
+                tma_load_4d(FP8 ? codes(g, 4) : slot(g, 4), &tm_kr, 0, k0 + i * BN, 8, b, done);
             }
             ++issued;
         }
@@ -442,49 +456,47 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t ID_QK = idesc_f16(FP8 ? 0u : 1u, 0, BM, BN);
-            constexpr uint32_t ID_PV = idesc_f16(FP8 ? 0u : 1u, 1, BM, 256);
+            constexpr uint32_t ID_QK = idesc_f16(1u, 0, BM, BN);
+            constexpr uint32_t ID_PV = idesc_f16(1u, 1, BM, 256);
             bool ok = mbar_wait(bar(C::B_QREADY), 0);
             tc_fence_after();
-            // PV_i as soon as P_i is ready (it frees tile group i % NG for the
-            // next load); otherwise QK_j once tile j has landed and the stagers
-            // have read S_{j-1}. Each test is on the next phase of its barrier
-            // (the previous one has completed, or the MMA that needs it would
-            // not have been issued), so a parity test cannot see a stale phase.
-            // An idle spell longer than 2 s gives up like every other wait.
-            int i = 0, j = 0;
+            // PV of half tile u as soon as its P is ready (the second half
+            // frees tile group u / 2 % NG for the next load); otherwise QK_j
+            // once tile j is ready and the stagers have read S_{j-1}. Each
+            // test is on the next phase of its barrier (the previous one has
+            // completed, or the MMA that needs it would not have been
+            // issued), so a parity test cannot see a stale phase. An idle
+            // spell longer than 2 s gives up like every other wait.
+            int u = 0, j = 0;
             uint64_t idle0 = 0;
-            while (ok && i < ntiles) {
+            while (ok && u < nunits) {
                 if (misc[1]) {
                     ok = false;
                     break;
                 }
-                if (j > i && mbar_test(bar(C::B_PFULL), (uint32_t)i & 1u)) {
-                    // O[128 x 256] += P_i[128 x 64] V_i[64 x 256]; frees tile group i % NG
+                if ((u >> 1) < j && mbar_test(bar(C::B_PFULL + (u & 1)), (uint32_t)(u >> 1) & 1u)) {
+                    // O[128 x 256] += P_u[128 x 32] V_u[32 x 256]: keys 32h..32h+31 of the tile
                     tc_fence_after();
-                    const uint64_t vb = desc_sw128(slot(i % NG, 0), KCH_BYTES, 1024);
-                    const uint32_t lo = (uint32_t)vb, hi = (uint32_t)(vb >> 32);
-                    if (i == 0)
-                        mma_ts<false>(tmem + TM_O, tmem + TM_P, lo, hi, ID_PV);
+                    const int g = (u >> 1) % NG, h = u & 1;
+                    const uint64_t vb = desc_sw128(slot(g, 0), KCH_BYTES, 1024);
+                    const uint32_t lo = (uint32_t)vb + 256u * (uint32_t)h, hi = (uint32_t)(vb >> 32);
+                    const uint32_t ap = tmem + TM_P + 16u * (uint32_t)h;
+                    if (u == 0)
+                        mma_ts<false>(tmem + TM_O, ap, lo, hi, ID_PV);
                     else
-                        mma_ts<true>(tmem + TM_O, tmem + TM_P, lo, hi, ID_PV);
-#pragma unroll
-                    for (int kk = 1; kk < 4; ++kk)  // 16 keys = 2048 bytes of V per step
-                        mma_ts<true>(tmem + TM_O, tmem + TM_P + 8u * kk, lo + 128u * kk, hi, ID_PV);
-                    mma_commit(bar(C::B_GEMPTY + i % NG));
-                    mma_commit(bar(C::B_PVDONE));
-                    ++i;
+                        mma_ts<true>(tmem + TM_O, ap, lo, hi, ID_PV);
+                    mma_ts<true>(tmem + TM_O, ap + 8u, lo + 128u, hi, ID_PV);  // 16 keys = 2 KB of V
+                    if (h) mma_commit(bar(C::B_GEMPTY + g));
+                    mma_commit(bar(C::B_PVDONE + h));
+                    ++u;
                     idle0 = 0;
                     continue;
                 }
                 if (j < ntiles && mbar_test(bar(C::B_GFULL + j % NG), (uint32_t)(j / NG) & 1u) &&
                     (j == 0 || mbar_test(bar(C::B_SFREE), (uint32_t)(j - 1) & 1u))) {
                     tc_fence_after();
-                    const uint64_t b0 = desc_sw128(slot(j % NG, lc0), 16, 1024);
-                    if (half)
-                        issue_qk<4>(tmem + TM_S, tmem + TM_Q, (uint32_t)b0, (uint32_t)(b0 >> 32), ID_QK);
-                    else
-                        issue_qk<5>(tmem + TM_S, tmem + TM_Q, (uint32_t)b0, (uint32_t)(b0 >> 32), ID_QK);
+                    const uint64_t b0 = desc_sw128(slot(j % NG, 0), 16, 1024);
+                    issue_qk(tmem + TM_S, tmem + TM_Q, (uint32_t)b0, (uint32_t)(b0 >> 32), ID_QK, half);
                     mma_commit(bar(C::B_SFULL));
                     ++j;
                     idle0 = 0;
@@ -503,7 +515,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             mbar_wait(bar(C::B_DRAIN), 0);
         }
     } else if (warp == 2) {
-        // ------------------------------------------------------------ key visibility, FP8 converter
+        // ------------------------------------------------------------ key visibility, row scales
         // Key j of a tile is seen by query token t iff its position is at most
         // L - T + t: store d = clamp(position - (L - T), 0, T), and d = T (seen
         // by none) for unresolved or absent entries; row t then masks d > t.
@@ -515,109 +527,71 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const int32_t *res_b = p.resolved + (size_t)b * p.K;
         const int32_t *top_b = p.topk + (size_t)b * p.K;
         const float *gs = (FP8 && !INPLACE) ? p.gscale + (size_t)b * p.K : nullptr;
+        int16_t *kvis = reinterpret_cast<int16_t *>(smem + C::OFF_KVIS);
+        float *ksc = reinterpret_cast<float *>(smem + C::OFF_KSC);
         bool ok = true;
         for (int i = 0; i < ntiles; ++i) {
             const int g = i % NG;
             const uint32_t ph = (uint32_t)(i / NG) & 1u;
-            // the slot's previous tile is finished (FP8: and this tile has landed)
-            if (ok)
-                ok = mbar_wait(bar(FP8 ? C::B_GLANDED + g : C::B_GEMPTY + g), FP8 ? ph : ph ^ 1u) &&
-                     !misc[1];
-            int res[2], top[2];
-            float sc[2];
+            // the slot's previous tile is finished (its stagers and softmax read these rings)
+            if (ok) ok = mbar_wait(bar(C::B_GEMPTY + g), ph ^ 1u) && !misc[1];
+            int dm[2] = {0, 0};
 #pragma unroll
             for (int h = 0; h < 2; ++h) {  // keys lane and lane + 32; loads issued together
                 const int j = k0 + i * BN + lane + 32 * h;
                 const bool in = j < k1;
-                res[h] = in ? res_b[j] : -1;
-                top[h] = in ? top_b[j] : 0;
-                sc[h] = 0.f;
-                if (FP8)
-                    sc[h] = INPLACE ? (res[h] >= 0 ? p.pool_scales[res[h]] : 0.f)
-                                    : (j < p.K ? gs[j] : 0.f);
-            }
-            if (FP8) {
-                __half2 s2[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) s2[h] = __float2half2_rn(sc[h]);
-                for (int lc = 0; lc < NLC; ++lc) {
-                    // The codes of all five chunks sit packed in the upper half of
-                    // the group. Chunk lc's f16 rows overlap only the codes of
-                    // chunks <= lc, so in ascending order with all of a chunk's
-                    // codes read before any of its f16 rows is written, nothing
-                    // is overwritten before it has been read.
-                    const uint32_t sl = slot(g, lc);
-                    uint4 raw4[2][4];
-                    if (ok) {
-#pragma unroll
-                        for (int h = 0; h < 2; ++h)
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                raw4[h][q] = ld_shared_v4(codes(g, lc) + (lane + 32 * h) * 64 + 16 * q);
-                    }
-                    __syncwarp();
-                    if (!ok) continue;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int ct = lane + 32 * h;
-                        const uint32_t dst = sl + ct * 128;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {  // 16 codes -> 16 f16 = two 16-byte chunks
-                            const uint32_t w[4] = {raw4[h][q].x, raw4[h][q].y, raw4[h][q].z,
-                                                   raw4[h][q].w};
-                            uint32_t hv[8];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                hv[2 * e] = hmul2_u32(e4m3x2_to_f16x2(w[e] & 0xffffu), s2[h]);
-                                hv[2 * e + 1] = hmul2_u32(e4m3x2_to_f16x2(w[e] >> 16), s2[h]);
-                            }
-                            st_shared_v4(dst + (((2 * q) ^ (ct & 7)) << 4), hv[0], hv[1], hv[2], hv[3]);
-                            st_shared_v4(dst + (((2 * q + 1) ^ (ct & 7)) << 4), hv[4], hv[5], hv[6],
-                                         hv[7]);
-                        }
-                    }
-                }
-                if (ok) {
-                    fence_proxy_async();
-                    mbar_arrive(bar(C::B_GFULL + g));
-                }
-            }
-            int dm = 0;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                long long d = (long long)top[h] - first;
+                const int res = in ? res_b[j] : -1;
+                const int top = in ? top_b[j] : 0;
+                long long d = (long long)top - first;
                 d = d < 0 ? 0 : (d > p.T ? p.T : d);
-                const int v = res[h] >= 0 ? (int)d : p.T;
-                dm = max(dm, v);
-                if (ok) kvis[g * BN + lane + 32 * h] = (int16_t)v;
+                const int v = res >= 0 ? (int)d : p.T;
+                dm[h] = v;
+                if (ok) {
+                    kvis[g * BN + lane + 32 * h] = (int16_t)v;
+                    if (FP8) {
+                        float sc = 0.f;
+                        if (res >= 0) sc = INPLACE ? p.pool_scales[res] : gs[j];
+                        ksc[g * BN + lane + 32 * h] = sc;
+                    }
+                }
             }
-            // the largest d of the tile: rows with t >= it skip the mask
-            dm = __reduce_max_sync(0xffffffffu, dm);
-            if (ok && lane == 0) tdmax[g] = dm;
+            // the largest d of each half tile: rows with t >= it skip the mask
+            const int d0 = __reduce_max_sync(0xffffffffu, dm[0]);
+            const int d1 = __reduce_max_sync(0xffffffffu, dm[1]);
+            if (ok && lane == 0) {
+                tdmax[2 * g] = d0;
+                tdmax[2 * g + 1] = d1;
+            }
             mbar_arrive(bar(C::B_KVIS + g));
         }
         if (!ok) fail();
     } else if (warp == 3) {
         // ------------------------------------------------------------ courier
-        // Sends each staged partial to the peer, in tile order, and arms this
-        // CTA's barrier for the peer's partial of the same tile.
+        // Sends each staged half tile to the peer, in order, once the peer has
+        // read the half tile sent two before into the same buffer; arms this
+        // CTA's barrier for the peer's partial of the same half tile; tells
+        // the stagers when the copy has read X_out.
         if (lane == 0) {
             const uint32_t peer_xin = hs::dsmem_map(smem + C::OFF_XIN, peer);
             const uint32_t peer_xfull = hs::dsmem_map(smem + C::OFF_BAR + 8 * C::B_XFULL, peer);
             bool ok = true;
-            auto send = [&](int j) {
-                const uint32_t x = (uint32_t)(j & 1);
-                if (ok) ok = mbar_wait(bar(C::B_STAGED + x), (uint32_t)(j >> 1) & 1u);
+            for (int u = 0; u < nunits; ++u) {
+                const uint32_t x = (uint32_t)(u & 1);
+                if (ok) ok = mbar_wait(bar(C::B_STAGED + x), (uint32_t)(u >> 1) & 1u);
+                if (ok && u >= 2)
+                    ok = mbar_wait_cluster(bar(C::B_XTAKEN + x), (uint32_t)((u - 2) >> 1) & 1u);
                 if (ok && !misc[1]) {
-                    mbar_expect_tx(bar(C::B_XFULL + x), X_BYTES);  // arms this CTA's receive of tile j
+                    mbar_expect_tx(bar(C::B_XFULL + x), X_BYTES);  // arms this CTA's receive of u
                     asm volatile(
                         "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes"
                         " [%0], [%1], %2, [%3];" ::"r"(peer_xin + x * X_BYTES),
                         "r"(sXout + x * X_BYTES), "r"((uint32_t)X_BYTES), "r"(peer_xfull + 8u * x)
                         : "memory");
+                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
                 }
-            };
-            for (int j = 0; j < ntiles; ++j) send(j);
+                mbar_arrive(bar(C::B_XOUTDONE + x));
+            }
             if (!ok) fail();
         }
     } else {
@@ -629,19 +603,32 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         bool ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_QFULL), 0));
         if (ok) {
-            // this thread's row of staged Q chunks into its TMEM lane: stagers
-            // even chunks, softmax threads odd ones
-            for (int c = stager ? 0 : 1; c < nq; c += 2) {
+            // this thread's row of the staged Q into its TMEM lane: stagers
+            // value chunks 0 and 2 and this CTA's half of the rope chunk,
+            // softmax threads value chunks 1 and 3
+            for (int c = stager ? 0 : 1; c < 4; c += 2) {
                 uint32_t q[32];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const uint4 v = ld_shared_v4(sQst + c * QCH_BYTES + x_off(row, u));
-                    q[4 * u] = FP8 ? bf16x2_to_f16x2(v.x) : v.x;
-                    q[4 * u + 1] = FP8 ? bf16x2_to_f16x2(v.y) : v.y;
-                    q[4 * u + 2] = FP8 ? bf16x2_to_f16x2(v.z) : v.z;
-                    q[4 * u + 3] = FP8 ? bf16x2_to_f16x2(v.w) : v.w;
+                    q[4 * u] = v.x;
+                    q[4 * u + 1] = v.y;
+                    q[4 * u + 2] = v.z;
+                    q[4 * u + 3] = v.w;
                 }
                 HS_TMEM_ST32(tmem + lane_off + TM_Q + 32u * (uint32_t)c, q);
+            }
+            if (stager) {
+                uint32_t q[16];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint4 v = ld_shared_v4(sQst + 4 * QCH_BYTES + x_off(row, 4 * half + u));
+                    q[4 * u] = v.x;
+                    q[4 * u + 1] = v.y;
+                    q[4 * u + 2] = v.z;
+                    q[4 * u + 3] = v.w;
+                }
+                HS_TMEM_ST16(tmem + lane_off + TM_Q + 128u, q);
             }
             tmem_wait_st();
         }
@@ -650,13 +637,54 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         mbar_arrive(bar(C::B_QREADY));
 
         if (stager) {
-            // ------------------------------------------------ stagers
-            // Tile j: read the partial S from TMEM, free S, and write it as
-            // f16 of S * sm_scale * log2(e) to X_out[j & 1] once tile j - 2 is
-            // done with that buffer (read here and taken by the peer).
+            // ------------------------------------------------ stagers (FP8: and converters)
+            // FP8, tile i: read every code of the group (20 KB, ten 16-byte
+            // units per thread), wait until all stagers have read theirs,
+            // then write the BF16 rows of all five chunks over the group (the
+            // rows of a chunk overlap the codes of that chunk and of lower
+            // ones). Tiles 0 and 1 are converted first, tile j + 2 after tile
+            // j has been staged, so a tile is ready two tiles before its QK.
+            // Every stager reaches the named barrier on every converted tile.
+            auto convert = [&](int i) {
+                const int g = i % NG;
+                if (ok) ok = __all_sync(0xffffffffu,
+                                        mbar_wait(bar(C::B_GLANDED + g), (uint32_t)(i / NG) & 1u) &&
+                                            !misc[1]);
+                uint4 cw[CVT_UNITS];
+                if (ok) {
+#pragma unroll
+                    for (int k = 0; k < CVT_UNITS; ++k)
+                        cw[k] = ld_shared_v4(codes(g, 0) + 16u * (row + NCVT * k));
+                }
+                named_bar_sync(3, NCVT);
+                if (ok) {
+#pragma unroll
+                    for (int k = 0; k < CVT_UNITS; ++k) {
+                        const int u = row + NCVT * k;  // 16-byte unit of codes: chunk, key, part
+                        const int lc = u >> 8, key = (u >> 2) & 63, part = u & 3;
+                        uint32_t o[8];
+                        e4m3x4_to_bf16(cw[k].x, o[0], o[1]);
+                        e4m3x4_to_bf16(cw[k].y, o[2], o[3]);
+                        e4m3x4_to_bf16(cw[k].z, o[4], o[5]);
+                        e4m3x4_to_bf16(cw[k].w, o[6], o[7]);
+                        const uint32_t dst = slot(g, lc) + key * 128;
+                        st_shared_v4(dst + (((2 * part) ^ (key & 7)) << 4), o[0], o[1], o[2], o[3]);
+                        st_shared_v4(dst + (((2 * part + 1) ^ (key & 7)) << 4), o[4], o[5], o[6], o[7]);
+                    }
+                    fence_proxy_async();  // the MMAs read these rows
+                }
+                mbar_arrive(bar(C::B_GFULL + g));
+            };
+            if (FP8) {
+                for (int i = 0; i < 2 && i < ntiles; ++i) convert(i);
+            }
+            // Tile j: read the partial S from TMEM, free S, and write each
+            // half (32 keys) as f32 of S * sm_scale * log2(e) (times the row
+            // scale for FP8) to X_out[u & 1] once half tile u - 2 is done
+            // with that buffer (read by this CTA's softmax and copied out).
             for (int j = 0; j < ntiles; ++j) {
-                const uint32_t x = (uint32_t)(j & 1);
-                uint32_t pk[32];
+                const int g = j % NG;
+                float sv[64];
                 if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SFULL), (uint32_t)j & 1u));
                 if (ok) {
                     tc_fence_after();
@@ -666,29 +694,53 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     HS_TMEM_WAIT_LD32(ra);
                     HS_TMEM_WAIT_LD32(rb);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        pk[e] = pack2<true>(__uint_as_float(ra[2 * e]) * p.scale_log2,
-                                            __uint_as_float(ra[2 * e + 1]) * p.scale_log2);
-                        pk[16 + e] = pack2<true>(__uint_as_float(rb[2 * e]) * p.scale_log2,
-                                                 __uint_as_float(rb[2 * e + 1]) * p.scale_log2);
+                    for (int e = 0; e < 32; ++e) {
+                        sv[e] = __uint_as_float(ra[e]);
+                        sv[32 + e] = __uint_as_float(rb[e]);
                     }
                 }
                 tc_fence_before();
                 mbar_arrive(bar(C::B_SFREE));  // QK of tile j + 1 may overwrite S
-                if (ok && j >= 2) {
-                    const uint32_t ph = (uint32_t)((j - 2) >> 1) & 1u;
-                    ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_READ + x), ph) &&
-                                                     mbar_wait(bar(C::B_XTAKEN + x), ph));
-                }
+                if (FP8 && ok)
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_KVIS + g), (uint32_t)(j / NG) & 1u));
                 if (ok) {
-                    const uint32_t xo = sXout + x * X_BYTES;
+                    if (FP8) {
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        st_shared_v4(xo + x_off(row, c), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-                                     pk[4 * c + 3]);
-                    fence_proxy_async();  // the courier's bulk copy reads it
+                        for (int q = 0; q < 16; ++q) {
+                            const float4 s4 = ld_shared_f4(sKsc + (uint32_t)(g * BN * 4 + 16 * q));
+                            sv[4 * q] *= p.scale_log2 * s4.x;
+                            sv[4 * q + 1] *= p.scale_log2 * s4.y;
+                            sv[4 * q + 2] *= p.scale_log2 * s4.z;
+                            sv[4 * q + 3] *= p.scale_log2 * s4.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 64; ++e) sv[e] *= p.scale_log2;
+                    }
                 }
-                mbar_arrive(bar(C::B_STAGED + x));
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int u = 2 * j + h;
+                    const uint32_t x = (uint32_t)(u & 1);
+                    if (ok && u >= 2) {
+                        // X_out[x] was read by this CTA's softmax and by the copy to the peer
+                        const uint32_t ph = (uint32_t)((u - 2) >> 1) & 1u;
+                        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_READ + x), ph) &&
+                                                         mbar_wait(bar(C::B_XOUTDONE + x), ph));
+                    }
+                    if (ok) {
+                        const uint32_t xo = sXout + x * X_BYTES;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            st_shared_v4(xo + x_off(row, c), __float_as_uint(sv[32 * h + 4 * c]),
+                                         __float_as_uint(sv[32 * h + 4 * c + 1]),
+                                         __float_as_uint(sv[32 * h + 4 * c + 2]),
+                                         __float_as_uint(sv[32 * h + 4 * c + 3]));
+                        fence_proxy_async();  // the courier's bulk copy reads it
+                    }
+                    mbar_arrive(bar(C::B_STAGED + x));
+                }
+                if (FP8 && j + 2 < ntiles) convert(j + 2);
             }
         } else {
             // ------------------------------------------------ softmax, PV, epilogue
@@ -697,50 +749,49 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const int t = vrow ? mg / p.H : 0;  // query token of this row
             const uint32_t peer_xtaken = hs::dsmem_map(smem + C::OFF_BAR + 8 * C::B_XTAKEN, peer);
             float m2 = -INFINITY, l = 0.f;
-            // Every softmax thread runs every iteration and reaches every named
-            // barrier (those are not bounded in time); after a failed wait the
-            // remaining work is skipped.
-            for (int i = 0; i < ntiles; ++i) {
-                const uint32_t x = (uint32_t)(i & 1);
-                const int g = i % NG;
-                float s[64];
-                if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_XFULL + x), (i >> 1) & 1));
+            // Every softmax thread runs every half tile and reaches every
+            // named barrier (those are not bounded in time); after a failed
+            // wait the remaining work is skipped.
+            for (int u = 0; u < nunits; ++u) {
+                const uint32_t x = (uint32_t)(u & 1);
+                const int j = u >> 1, h = u & 1, g = j % NG;
+                float s[32];
+                if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_XFULL + x), (u >> 1) & 1));
                 if (ok) {
-                    // S = own partial + the peer's partial, both as sent
+                    // S = own partial + the peer's partial; f32 addition is
+                    // commutative, so the peer, adding them the other way
+                    // round, gets the same bits
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
-                        const uint4 a = ld_shared_v4(sXout + x * X_BYTES + x_off(row, c));
-                        const uint4 v = ld_shared_v4(sXin + x * X_BYTES + x_off(row, c));
-                        const float2 s0 = add_f16x2_f32(a.x, v.x), s1 = add_f16x2_f32(a.y, v.y);
-                        const float2 s2 = add_f16x2_f32(a.z, v.z), s3 = add_f16x2_f32(a.w, v.w);
-                        s[8 * c] = s0.x;
-                        s[8 * c + 1] = s0.y;
-                        s[8 * c + 2] = s1.x;
-                        s[8 * c + 3] = s1.y;
-                        s[8 * c + 4] = s2.x;
-                        s[8 * c + 5] = s2.y;
-                        s[8 * c + 6] = s3.x;
-                        s[8 * c + 7] = s3.y;
+                        const float4 a = ld_shared_f4(sXout + x * X_BYTES + x_off(row, c));
+                        const float4 v = ld_shared_f4(sXin + x * X_BYTES + x_off(row, c));
+                        s[4 * c] = a.x + v.x;
+                        s[4 * c + 1] = a.y + v.y;
+                        s[4 * c + 2] = a.z + v.z;
+                        s[4 * c + 3] = a.w + v.w;
                     }
                 }
                 // X_in[x] and X_out[x] read by every softmax thread: one thread
                 // frees X_out[x] for the stagers and X_in[x] for the peer
                 named_bar_sync(2, NSFT);
-                if (threadIdx.x == 256) {
+                if (threadIdx.x == 8 * 32) {
+                    // the reads above have returned their values, so an arrive
+                    // without a cluster-scope release (which would wait for a
+                    // cluster-wide fence) is enough to let the peer overwrite
                     mbar_arrive(bar(C::B_READ + x));
                     mbar_arrive_peer(peer_xtaken + 8u * x);
                 }
-                if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_KVIS + g), (uint32_t)(i / NG) & 1u));
-                uint32_t pk[32];
+                if (ok && h == 0)
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_KVIS + g), (uint32_t)(j / NG) & 1u));
+                uint32_t pk[16];
                 float alpha = 1.f;
                 bool need = false;
                 if (ok) {
-                    if (!__all_sync(0xffffffffu, tdmax[g] <= t)) {
-                        // some key of this tile is hidden from some row of this warp
-                        const uint32_t ka = hs::smem_addr(kvis + g * BN);
+                    if (!__all_sync(0xffffffffu, tdmax[2 * g + h] <= t)) {
+                        // some key of this half tile is hidden from some row of this warp
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) {  // 8 keys per 16 bytes, lower key in the low half
-                            const uint4 kv = ld_shared_v4(ka + 16 * q);
+                        for (int q = 0; q < 4; ++q) {  // 8 keys per 16 bytes, lower key in the low half
+                            const uint4 kv = ld_shared_v4(sKvis + (uint32_t)(g * BN * 2 + 64 * h + 16 * q));
                             const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
@@ -750,17 +801,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             }
                         }
                     }
-                    // tree reductions: no long dependency chains
-                    float mx[16];
+                    // tree reduction: no long dependency chain
+                    float mx[8];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        mx[e] = fmaxf(fmaxf(s[e], s[e + 16]), fmaxf(s[e + 32], s[e + 48]));
+                    for (int e = 0; e < 8; ++e)
+                        mx[e] = fmaxf(fmaxf(s[e], s[e + 8]), fmaxf(s[e + 16], s[e + 24]));
 #pragma unroll
-                    for (int w = 8; w >= 1; w >>= 1)
+                    for (int w = 4; w >= 1; w >>= 1)
 #pragma unroll
                         for (int e = 0; e < w; ++e) mx[e] = fmaxf(mx[e], mx[e + w]);
                     const float tmax = mx[0];
-                    if (i == 0) {
+                    if (u == 0) {
                         m2 = tmax;
                     } else if (tmax > m2 + TAU2) {
                         need = true;
@@ -769,22 +820,39 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         m2 = tmax;
                     }
                     const float mref = (m2 == -INFINITY) ? 0.f : m2;
-                    float ls[8];
+                    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (FP8) {
+                        // P = probability x the key's row scale (the value rows are codes)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) ls[e] = 0.f;
+                        for (int q = 0; q < 8; ++q) {
+                            const float4 s4 = ld_shared_f4(sKsc + (uint32_t)(g * BN * 4 + 128 * h + 16 * q));
+                            const float a0 = exp2f(s[4 * q] - mref), a1 = exp2f(s[4 * q + 1] - mref);
+                            const float a2 = exp2f(s[4 * q + 2] - mref), a3 = exp2f(s[4 * q + 3] - mref);
+                            ls[q & 3] += (a0 + a1) + (a2 + a3);
+                            pk[2 * q] = pack_bf16(a0 * s4.x, a1 * s4.y);
+                            pk[2 * q + 1] = pack_bf16(a2 * s4.z, a3 * s4.w);
+                        }
+                    } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float a = exp2f(s[2 * e] - mref), c = exp2f(s[2 * e + 1] - mref);
-                        ls[e & 7] += a + c;
-                        pk[e] = pack2<FP8>(a, c);
+                        for (int e = 0; e < 16; ++e) {
+                            const float a = exp2f(s[2 * e] - mref), c = exp2f(s[2 * e + 1] - mref);
+                            ls[e & 3] += a + c;
+                            pk[e] = pack_bf16(a, c);
+                        }
                     }
-                    l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-                    // P and O are free once PV of the previous tile has finished
-                    if (i > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_PVDONE), (uint32_t)(i - 1) & 1u));
+                    l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                    // this half's P columns were last read by PV of u - 2
+                    if (u >= 2)
+                        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_PVDONE + h),
+                                                               (uint32_t)((u - 2) >> 1) & 1u));
+                    // a rescale of O needs every earlier PV done (PV of u - 1 is the last)
+                    if (ok && u >= 1 && __any_sync(0xffffffffu, need))
+                        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_PVDONE + (h ^ 1)),
+                                                               (uint32_t)((u - 1) >> 1) & 1u));
                 }
                 if (ok) {
                     tc_fence_after();
-                    HS_TMEM_ST32(tmem + lane_off + TM_P, pk);
+                    HS_TMEM_ST16(tmem + lane_off + TM_P + 16u * (uint32_t)h, pk);
                     if (__any_sync(0xffffffffu, need)) {
 #pragma unroll 1
                         for (int cc = 0; cc < 8; ++cc) {
@@ -801,49 +869,52 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     tmem_wait_st();
                 }
                 tc_fence_before();
-                mbar_arrive(bar(C::B_PFULL));  // P_i (and a rescaled O) complete in TMEM
+                mbar_arrive(bar(C::B_PFULL + h));  // P_u (and a rescaled O) complete in TMEM
             }
-            if (ok && ntiles > 0) {
+            if (ok && nunits > 0) {
                 // the last PV's completion covers every earlier one
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_PVDONE), (uint32_t)(ntiles - 1) & 1u));
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_PVDONE + ((nunits - 1) & 1)),
+                                                       (uint32_t)((nunits - 1) >> 1) & 1u));
                 tc_fence_after();
             }
             if (!ok) fail();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const size_t orow = (size_t)b * p.M + mg;
             if (ok) {
+                // O / l as BF16 through shared memory (the ring is idle once the
+                // last PV is done): this warp's 32 rows x 256 columns as four
+                // 64-column boxes in the 128-byte-swizzled layout, then four
+                // TMA stores (rows past M are clipped by the tensor map)
+                const uint32_t stg = sR + (uint32_t)wq * 16384u;
 #pragma unroll 1
                 for (int cc = 0; cc < 8; ++cc) {
                     uint32_t o[32];
                     HS_TMEM_LD32(tmem + lane_off + TM_O + 32 * cc, o);
                     HS_TMEM_WAIT_LD32(o);
-                    if (!vrow) continue;
-                    const int col = half * 256 + 32 * cc;
-                    if (p.nsplit == 1) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * 512 + col);
+                    const uint32_t box = stg + (uint32_t)(cc >> 1) * 4096u + (uint32_t)lane * 128u;
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint32_t w[4];
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t w[4];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                w[e] = pack2<false>(__uint_as_float(o[8 * q + 2 * e]) * inv,
-                                                    __uint_as_float(o[8 * q + 2 * e + 1]) * inv);
-                            dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
-                        }
-                    } else {
-                        uint4 *dst = reinterpret_cast<uint4 *>(
-                            p.ws_o + (((size_t)split * p.B + b) * p.M + mg) * 512 + col);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint32_t w[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                w[e] = pack2<true>(__uint_as_float(o[8 * q + 2 * e]) * inv,
-                                                   __uint_as_float(o[8 * q + 2 * e + 1]) * inv);
-                            dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
-                        }
+                        for (int e = 0; e < 4; ++e)
+                            w[e] = pack_bf16(__uint_as_float(o[8 * q + 2 * e]) * inv,
+                                             __uint_as_float(o[8 * q + 2 * e + 1]) * inv);
+                        const int c = (cc & 1) * 4 + q;
+                        st_shared_v4(box + (uint32_t)((c ^ (lane & 7)) << 4), w[0], w[1], w[2], w[3]);
                     }
                 }
+                fence_proxy_async();  // the TMA stores read what the threads wrote
+                __syncwarp();
+                if (lane == 0) {
+                    const int zb = p.nsplit == 1 ? b : split * p.B + b;
+                    for (int cg = 0; cg < 4; ++cg)
+                        tma_store_3d(&tm_o, stg + (uint32_t)cg * 4096u, half * 256 + cg * 64,
+                                     mt * BM + wq * 32, zb);
+                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                    // the stores have read shared memory before the CTA may exit
+                    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                }
+                __syncwarp();
             }
             if (vrow && half == 0) {
                 const float lse = (ok && l > 0.f) ? (m2 + __log2f(l)) * 0.69314718055994531f : -INFINITY;
@@ -864,7 +935,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
 // Merges the KV-split partials: out = sum_s w_s O_s / sum_s w_s, w_s = exp(lse_s - max).
 __global__ void __launch_bounds__(256)
-combine_kernel(const __half *__restrict__ ws_o, const float *__restrict__ ws_lse, int nsplit,
+combine_kernel(const __nv_bfloat16 *__restrict__ ws_o, const float *__restrict__ ws_lse, int nsplit,
                int rows, __nv_bfloat16 *__restrict__ out, float *__restrict__ lse) {
     grid_dep_wait();  // the decode grid's partials are complete
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -886,12 +957,10 @@ combine_kernel(const __half *__restrict__ ws_o, const float *__restrict__ ws_lse
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const uint2 u = src[lane + 32 * q];  // elements 4 (lane + 32 q) .. + 3
-                const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
-                const float2 c = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
-                acc[4 * q] += w * a.x;
-                acc[4 * q + 1] += w * a.y;
-                acc[4 * q + 2] += w * c.x;
-                acc[4 * q + 3] += w * c.y;
+                acc[4 * q] += w * __uint_as_float(u.x << 16);
+                acc[4 * q + 1] += w * __uint_as_float(u.x & 0xffff0000u);
+                acc[4 * q + 2] += w * __uint_as_float(u.y << 16);
+                acc[4 * q + 3] += w * __uint_as_float(u.y & 0xffff0000u);
             }
         }
     }
@@ -899,8 +968,8 @@ combine_kernel(const __half *__restrict__ ws_o, const float *__restrict__ ws_lse
     uint2 *dst = reinterpret_cast<uint2 *>(out + (size_t)row * 512);
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-        dst[lane + 32 * q] = make_uint2(pack2<false>(acc[4 * q] * inv, acc[4 * q + 1] * inv),
-                                        pack2<false>(acc[4 * q + 2] * inv, acc[4 * q + 3] * inv));
+        dst[lane + 32 * q] = make_uint2(pack_bf16(acc[4 * q] * inv, acc[4 * q + 1] * inv),
+                                        pack_bf16(acc[4 * q + 2] * inv, acc[4 * q + 3] * inv));
     if (lane == 0) lse[row] = wsum > 0.f ? mx + __logf(wsum) : -INFINITY;
 }
 
@@ -911,16 +980,16 @@ struct Plan {
 };
 
 int sm_count() {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (!cached[dev]) {
-        int n = 0;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (!n) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
             n = 148;
-        cached[dev] = n;
+        cached[dev].store(n, std::memory_order_relaxed);
     }
-    return cached[dev];
+    return n;
 }
 
 Plan make_plan(int B, int T, int H, int K) {
@@ -938,7 +1007,7 @@ Plan make_plan(int B, int T, int H, int K) {
     pl.nsplit = (K + pl.kps - 1) / pl.kps;
     if (pl.nsplit > 1) {
         const size_t rows = (size_t)pl.nsplit * B * pl.M;
-        pl.ws_o_bytes = (rows * 512 * sizeof(__half) + 255) & ~size_t(255);
+        pl.ws_o_bytes = (rows * 512 * sizeof(__nv_bfloat16) + 255) & ~size_t(255);
         pl.ws_bytes = pl.ws_o_bytes + ((rows * sizeof(float) + 255) & ~size_t(255));
     }
     return pl;
@@ -974,32 +1043,44 @@ bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, uint64_t 
 }
 
 // Rows of 9 chunks of 64 elements, as a 4-D map (element, row, chunk,
-// request) with a (64 x BN x NLC x 1) box.
+// request) with a (64 x BN x nchunks x 1) box.
 bool make_chunk_map(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, uint64_t rows,
-                    uint64_t batch, uint64_t row_bytes, uint64_t chunk_bytes, CUtensorMapSwizzle sw) {
+                    uint64_t batch, uint64_t row_bytes, uint64_t chunk_bytes, CUtensorMapSwizzle sw,
+                    uint32_t nchunks) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[4] = {64, rows, 9, batch};
     cuuint64_t strides[3] = {row_bytes, chunk_bytes, row_bytes * rows};
-    cuuint32_t box[4] = {64, (cuuint32_t)BN, (cuuint32_t)NLC, 1};
+    cuuint32_t box[4] = {64, (cuuint32_t)BN, nchunks, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     return fn(m, dt, 4, const_cast<void *>(ptr), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_NONE,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// cudaFuncSetAttribute once per device and kernel variant (the opt-in to
+// more than 48 KB of shared memory is per device).
 template <bool FP8, bool INPLACE>
-hs_status launch_decode(dim3 grid, cudaStream_t s, const CUtensorMap &tq, const CUtensorMap &tk,
-                        const DecParams &p) {
-    static bool ready = false;
-    if (!ready) {
-        HS_CUDA_TRY(cudaFuncSetAttribute(decode_tc_kernel<FP8, INPLACE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_ALLOC));
-        ready = true;
-    }
+hs_status set_smem_attr(int dev) {
+    static std::atomic<int> state[64];  // 0 unknown, 1 set
+    if (dev < 0 || dev >= 64) return HS_ERR_UNSUPPORTED;
+    if (state[dev].load(std::memory_order_acquire) == 1) return HS_OK;
+    HS_CUDA_TRY(cudaFuncSetAttribute(decode_tc_kernel<FP8, INPLACE>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_ALLOC));
+    state[dev].store(1, std::memory_order_release);
+    return HS_OK;
+}
+
+template <bool FP8, bool INPLACE>
+hs_status launch_decode(dim3 grid, cudaStream_t s, const CUtensorMap &tq, const CUtensorMap &tkv,
+                        const CUtensorMap &tkr, const CUtensorMap &to, const DecParams &p) {
+    int dev = 0;
+    HS_CUDA_TRY(cudaGetDevice(&dev));
+    const hs_status st = set_smem_attr<FP8, INPLACE>(dev);
+    if (st != HS_OK) return st;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(NTHR, 1, 1);
+    cfg.blockDim = dim3(Threads<FP8>::N, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_ALLOC;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
@@ -1012,7 +1093,7 @@ hs_status launch_decode(dim3 grid, cudaStream_t s, const CUtensorMap &tq, const 
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<FP8, INPLACE>, tq, tk, p) == cudaSuccess
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<FP8, INPLACE>, tq, tkv, tkr, to, p) == cudaSuccess
                ? HS_OK
                : HS_ERR_CUDA;
 }
@@ -1050,7 +1131,7 @@ hs_status decode_entry(hs_pool_t pool, int32_t B, int32_t T, int32_t tpl, int32_
         return HS_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    CUtensorMap tq, tk;
+    CUtensorMap tq, tkv, tkr;
     if (!make_map(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_q, hs::kDim, pl.M, B, 2 * hs::kDim, 64,
                   BM, CU_TENSOR_MAP_SWIZZLE_128B))
         return HS_ERR_CUDA;
@@ -1058,17 +1139,20 @@ hs_status decode_entry(hs_pool_t pool, int32_t B, int32_t T, int32_t tpl, int32_
     if (inplace) {
         // the pool as [rows][576] with one-row boxes, for four-row gathers
         const uint64_t nrows = (uint64_t)(pool->cfg.n_gpu_blocks + 1) * hs::kPage;
-        ok_k = fp8 ? make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, pool->d_rows, hs::kDim, nrows, 1,
+        ok_k = fp8 ? make_map(&tkv, CU_TENSOR_MAP_DATA_TYPE_UINT8, pool->d_rows, hs::kDim, nrows, 1,
                               hs::kDim, 64, 1, CU_TENSOR_MAP_SWIZZLE_NONE, 2)
-                   : make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pool->d_rows, hs::kDim, nrows, 1,
-                              2 * hs::kDim, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B, 2);
+                   : make_map(&tkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pool->d_rows, hs::kDim, nrows,
+                              1, 2 * hs::kDim, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B, 2);
+        tkr = tkv;
     } else {
-        // [B][K][9 chunks][64] viewed as (column, row, chunk, request) so that one
-        // box brings all five chunks of 64 rows, chunk-major in shared memory
-        ok_k = fp8 ? make_chunk_map(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, d_gathered, K, B, hs::kDim, 64,
-                                    CU_TENSOR_MAP_SWIZZLE_NONE)
-                   : make_chunk_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_gathered, K, B,
-                                    2 * hs::kDim, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+        // [B][K][9 chunks][64] viewed as (column, row, chunk, request): one box
+        // brings four value chunks of 64 rows (chunk-major in shared memory),
+        // another the rope chunk
+        const auto dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        const uint64_t rb = fp8 ? hs::kDim : 2 * hs::kDim, cb = fp8 ? 64 : 128;
+        const auto sw = fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
+        ok_k = make_chunk_map(&tkv, dt, d_gathered, K, B, rb, cb, sw, 4) &&
+               make_chunk_map(&tkr, dt, d_gathered, K, B, rb, cb, sw, 1);
     }
     if (!ok_k) return HS_ERR_CUDA;
 
@@ -1079,12 +1163,10 @@ hs_status decode_entry(hs_pool_t pool, int32_t B, int32_t T, int32_t tpl, int32_
     p.ctx = pool->d_ctx;
     p.gscale = d_gathered_scale;
     p.pool_scales = pool->d_scales;
-    p.gathered = static_cast<const uint8_t *>(d_gathered);
     p.zero_row = (int)(pool->cfg.n_gpu_blocks * hs::kPage);
-    p.row_bytes = fp8 ? hs::kDim : 2 * hs::kDim;
     p.out = static_cast<__nv_bfloat16 *>(d_out);
     p.lse = d_lse;
-    p.ws_o = pl.nsplit > 1 ? static_cast<__half *>(d_workspace) : nullptr;
+    p.ws_o = pl.nsplit > 1 ? static_cast<__nv_bfloat16 *>(d_workspace) : nullptr;
     p.ws_lse = pl.nsplit > 1
                    ? reinterpret_cast<float *>(static_cast<uint8_t *>(d_workspace) + pl.ws_o_bytes)
                    : nullptr;
@@ -1101,10 +1183,16 @@ hs_status decode_entry(hs_pool_t pool, int32_t B, int32_t T, int32_t tpl, int32_
     p.scale_log2 = sm_scale * 1.4426950408889634f;
 
     const dim3 grid(2 * pl.nsplit, pl.mtiles, B);
-    const hs_status st = fp8 ? (inplace ? launch_decode<true, true>(grid, s, tq, tk, p)
-                                        : launch_decode<true, false>(grid, s, tq, tk, p))
-                             : (inplace ? launch_decode<false, true>(grid, s, tq, tk, p)
-                                        : launch_decode<false, false>(grid, s, tq, tk, p));
+    // the output (one split) or the split partials, [batch][M][512] BF16, in
+    // 64-column x 32-row boxes
+    CUtensorMap to;
+    if (!make_map(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pl.nsplit == 1 ? d_out : d_workspace, 512,
+                  pl.M, (uint64_t)B * pl.nsplit, 1024, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+        return HS_ERR_CUDA;
+    const hs_status st = fp8 ? (inplace ? launch_decode<true, true>(grid, s, tq, tkv, tkr, to, p)
+                                        : launch_decode<true, false>(grid, s, tq, tkv, tkr, to, p))
+                             : (inplace ? launch_decode<false, true>(grid, s, tq, tkv, tkr, to, p)
+                                        : launch_decode<false, false>(grid, s, tq, tkv, tkr, to, p));
     if (st != HS_OK) return st;
     if (pl.nsplit > 1) {
         const int rows = B * pl.M;
@@ -1117,7 +1205,7 @@ hs_status decode_entry(hs_pool_t pool, int32_t B, int32_t T, int32_t tpl, int32_
         ca[0].val.programmaticStreamSerializationAllowed = 1;
         cc.attrs = ca;
         cc.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cc, combine_kernel, (const __half *)p.ws_o, (const float *)p.ws_lse,
+        if (cudaLaunchKernelEx(&cc, combine_kernel, (const __nv_bfloat16 *)p.ws_o, (const float *)p.ws_lse,
                                pl.nsplit, rows, p.out, d_lse) != cudaSuccess)
             return HS_ERR_CUDA;
     }
@@ -1158,7 +1246,10 @@ extern "C" hs_status hs_sparse_mla_decode_per_token(
 static __device__ __align__(256) unsigned char hs_static_decode_ws[HS_STATIC_DECODE_WS_BYTES];
 
 namespace {
-void *g_static_ws[64];  // device address of hs_static_decode_ws, looked up once per device
+// device address of hs_static_decode_ws, looked up once per device (the
+// lookup is idempotent, so two threads racing on a first call store the same
+// address)
+std::atomic<void *> g_static_ws[64];
 }
 
 extern "C" hs_status hs_sparse_mla_decode_static_ws(
@@ -1172,16 +1263,16 @@ extern "C" hs_status hs_sparse_mla_decode_static_ws(
     int dev = 0;
     HS_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return HS_ERR_UNSUPPORTED;
-    if (!g_static_ws[dev]) {
+    void *ws = g_static_ws[dev].load(std::memory_order_acquire);
+    if (!ws) {
         // host code cannot use the array's name as a device address: ask the
         // runtime for this device's copy (the current device)
-        void *p = nullptr;
-        HS_CUDA_TRY(cudaGetSymbolAddress(&p, hs_static_decode_ws));
-        if (!p) return HS_ERR_CUDA;
-        g_static_ws[dev] = p;
+        HS_CUDA_TRY(cudaGetSymbolAddress(&ws, hs_static_decode_ws));
+        if (!ws) return HS_ERR_CUDA;
+        g_static_ws[dev].store(ws, std::memory_order_release);
     }
     return hs_sparse_mla_decode(pool, B, T, H, K, d_q, d_gathered, d_gathered_scale, d_resolved,
-                                d_topk_idx, d_req_ids, sm_scale, d_out, d_lse, g_static_ws[dev],
+                                d_topk_idx, d_req_ids, sm_scale, d_out, d_lse, ws,
                                 HS_STATIC_DECODE_WS_BYTES, stream);
 }
 
