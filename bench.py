@@ -133,6 +133,19 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def run_config(desc, w, ws, layers=1, in_place=False):
+    """The line's config: the workload and how it is run (the same dict for
+    the GPU arm and the CPU-oracle arm on the headline workload)."""
+    return {"workload": desc, "global_batch": w.B * ws, "top_k": w.K, "layers": layers,
+            "heads": w.H, "query_tokens": w.T, "ctx": w.ctx,
+            "parallelism": f"replicas x{ws} (requests sharded by rank, no collective)",
+            "rows": ("read in place from the pool by attention (no gathered buffer)"
+                     if in_place else "gathered by the resolve, then read by attention"),
+            "l2": ("GPU arm: flushed before every timed step, 256 MiB written then 256 MiB of "
+                   "other data read (clean, cold L2), the flush outside the events; CPU-oracle "
+                   "arm: not applicable")}
+
+
 def algorithmic(w, counts_sum, in_place=False, per_token=None):
     """Algorithmic bytes / flops of one step (per-unit figures x units).
 
@@ -199,22 +212,18 @@ def _link_peak_gbs(to_host: bool = False):
     return best
 
 
-def run_gpu(args):
+def measure(args, name, steps, with_e2e=False):
+    """Times `steps` decode steps of workload `name` (resolve + decode per
+    step, CUDA events on the launching stream, cold L2) and returns the
+    bench line's fields for it. with_e2e adds the end-to-end figure through
+    the C ABI with host buffers."""
     import numpy as np
     import torch
-
-    ws, rank, local = _dist()
-    torch.cuda.set_device(local)
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    import __graft_entry__ as g
-    g.build()
     import tiered_sparse_mla_gb300 as hs
     import workloads as W
     from harness import GpuAgent, GpuWorkload
 
-    name = args.workload
+    ws, rank, local = _dist()
     agent = name == "agent"
     w = W.AgentMix() if agent else W.WORKLOADS[name]
     if args.batch and args.batch != w.B:
@@ -223,7 +232,6 @@ def run_gpu(args):
         # a shorter context keeps the decode work (K rows per request) and
         # shrinks the pool, for profiler captures; not a bench line
         w = w.scaled(ctx=args.ctx)
-    steps = args.steps or DEFAULT_STEPS[name]
     per_token = bool(args.per_token)
     if per_token and (agent or w.T < 2):
         raise SystemExit("--per-token needs a workload with several query tokens (hybrid)")
@@ -397,12 +405,21 @@ def run_gpu(args):
     if t_flops > t_bytes:
         kernels["decode"].update(bound="tensor", achieved=flops / (dec_ms * 1e-3) / 1e12,
                                  unit="TFLOP/s", peak=tf_peak)
+    # the resolve's roofline time is max(HBM bytes / BW, miss bytes / host-link BW)
+    link_peak = _link_peak_gbs() if r_link > 0 else None
+    if r_link > 0 and r_link / (link_peak * 1e9) > r_hbm / (hbm_peak * 1e9):
+        kernels["resolve"].update(bound="host-link", achieved=r_link / (res_ms * 1e-3) / 1e9,
+                                  peak=round(link_peak, 1), bytes_per_launch=r_link,
+                                  hbm_bytes_per_launch=r_hbm)
     top = max(kernels, key=lambda k: kernels[k]["ms"])
     kt = kernels[top]
+    src = (f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback")
+    if kt["bound"] == "host-link":
+        src = "measured live: pinned 256 MiB host-to-device copy"
     roofline = {"kernel": top, "bound": kt["bound"], "achieved": round(kt["achieved"], 1),
                 "peak": kt["peak"], "unit": kt["unit"],
                 "frac": round(kt["achieved"] / kt["peak"], 4), "traffic": kt["traffic"],
-                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"}
+                "peak_source": src}
 
     launches = 1 + L * (1 + (1 if (hs.hs_decode_workspace_bytes(w.B * w.T, 1, w.H, w.K) if per_token
                                    else hs.hs_decode_workspace_bytes(w.B, w.T, w.H, w.K)) > 0 else 0))
@@ -419,15 +436,9 @@ def run_gpu(args):
         "metric": METRIC, "value": round(steps_per_s, 2), "unit": "decode steps/s",
         "n_gpus": ws, "steps": steps, "warmup": args.warmup,
         "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "fp8 rows, f16 MMA",
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "fp8 rows, bf16 MMA",
         "data": "synthetic",
-        "config": {"workload": desc, "global_batch": w.B * ws, "top_k": w.K, "layers": L,
-                   "heads": w.H, "query_tokens": w.T, "ctx": w.ctx,
-                   "parallelism": f"replicas x{ws} (requests sharded by rank, no collective)",
-                   "rows": ("read in place from the pool by attention (no gathered buffer)"
-                            if args.in_place else "gathered by the resolve, then read by attention"),
-                   "l2": ("flushed before every timed step: 256 MiB written, then 256 MiB of "
-                          "other data read (clean, cold L2); the flush is outside the events")},
+        "config": run_config(desc, w, ws, L, args.in_place),
         "resolved_rows_per_s": round(rows_per_s, 1),
         "resolve_ms": round(res_ms, 5), "decode_ms": round(dec_ms, 5),
         "counts_per_step": {"resident": float(per_step_counts[0]), "hot": float(per_step_counts[1]),
@@ -441,7 +452,6 @@ def run_gpu(args):
         "clocks": clk.summary(), "wall_s": round(wall, 3),
     }
     if r_link > 0:
-        link_peak = _link_peak_gbs()
         ach = r_link / (res_ms * 1e-3) / 1e9
         line["host_link"] = {"miss_bytes_per_step": r_link, "achieved": round(ach, 1),
                              "peak": round(link_peak, 1), "unit": "GB/s",
@@ -454,17 +464,57 @@ def run_gpu(args):
             if a < b:
                 per_turn.append(round(sum(t_res[a:b]) + sum(t_dec[a:b]), 3))
         line["per_turn_ms"] = per_turn
-    if name == WORKLOAD and not agent and L == 1:
+    if with_e2e and not agent and L == 1:
         line["e2e"] = run_e2e(args, gw, qs, stream, w)
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline and name == WORKLOAD and L == 1:
-        line["cpu_baseline"] = cpu_baseline(w, args)
-    if rank == 0:
-        print(json.dumps(line), flush=True)
     if group is not None:
         hs.hs_layer_group_destroy(group)
     for x in gws:
         x.pool.close()
+    torch.cuda.synchronize()
+    return line, w
+
+
+# Configurations measured after the headline in the default run (one object
+# per configuration in the same JSON line); the agent mix runs all its steps.
+PER_CONFIG = ["tiny", "hybrid", "noresident", "agent"]
+PER_CONFIG_KEYS = ("value", "unit", "steps", "ms_per_step", "resolved_rows_per_s", "resolve_ms",
+                   "decode_ms", "counts_per_step", "roofline", "kernels", "host_link", "clocks",
+                   "per_turn_ms", "dtype")
+
+
+def run_gpu(args):
+    import torch
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
     if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    import __graft_entry__ as g
+    g.build()
+    plain = args.layers <= 1 and not args.in_place and not args.per_token and not args.batch \
+        and not args.ctx
+    headline = args.workload == WORKLOAD and plain
+    line, w = measure(args, args.workload, args.steps, with_e2e=headline or args.workload == WORKLOAD)
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and args.workload == WORKLOAD \
+            and args.layers <= 1:
+        line["cpu_baseline"] = cpu_baseline(w, args)
+    if headline and not args.no_per_config:
+        per = {}
+        for name in PER_CONFIG:
+            n_steps = DEFAULT_STEPS[name] if name == "agent" else max(args.steps, 32)
+            torch.cuda.empty_cache()
+            sub, wn = measure(args, name, n_steps)
+            entry = {k: sub[k] for k in PER_CONFIG_KEYS if k in sub}
+            entry["workload"] = sub["config"]["workload"]
+            if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+                entry["cpu_baseline"] = cpu_baseline_config(name, wn, args)
+            per[name] = entry
+        line["per_config"] = per
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
         dist.destroy_process_group()
 
 
@@ -678,10 +728,86 @@ def cpu_baseline(w, args):
         spent += m
         s += 1
     v = len(per) / sum(per)
+    # the same oracle on one core: one step of a one-request sub-batch, its
+    # resolve and the attention of 32 query rows, extrapolated the same way
+    one = OracleSampler(w, 1, 1)
+    e1, m1, _, _ = one.step(0, 32)
     return {"value": round(v, 5), "unit": "decode steps/s", "cores": threads, "kind": "oracle",
             "sample": (f"{s} decode steps of a {n_req}-request sub-batch of the same workload "
                        f"(resolve and attention of all {n_req * w.T * w.H} query rows), "
-                       f"extrapolated to {w.B} requests; {spent:.1f} s of CPU work")}
+                       f"extrapolated to {w.B} requests; {spent:.1f} s of CPU work"),
+            "value_1core": round(1.0 / e1, 6),
+            "sample_1core": (f"1 core: one step of a 1-request sub-batch (resolve, attention of 32 "
+                             f"query rows) extrapolated to {w.B} requests; {m1:.1f} s of CPU work")}
+
+
+def cpu_baseline_config(name, w, args, budget_s=4.0):
+    """The oracle as it stands on a bounded sample of configuration `name`:
+    one request of the configuration's shape with its own seeded lists
+    (pool rows N(0,1); host rows zero: the resolve copies them all the same),
+    whose resolve is timed over the first steps and whose attention is timed
+    on a sample of query rows, both extrapolated to the full batch. For the
+    agent mix the request is a hybrid-shaped one at the mix's first-turn
+    context (every step's attention has the same shape: FP8, 4 query
+    tokens, 128 heads, top-2048)."""
+    import numpy as np
+    import torch
+    import oracle
+    import workloads as W
+    oracle.build()
+    threads = oracle.max_threads()
+    B = w.B
+    if name == "agent":
+        w1 = W.WORKLOADS["hybrid"].scaled(B=1, ctx=w.first, index=w.index if hasattr(w, "index")
+                                          else 4)
+        label = (f"a hybrid-shaped request (FP8, 4 tokens, 128 heads, top-2048) at the mix's "
+                 f"first-turn context {w.first}")
+    else:
+        w1 = w.scaled(B=1)
+        label = f"one request of the same shape ({w.ctx}-token context)"
+    lay = W.layout(w1)
+    rows = torch.empty((lay.n_gpu_blocks * 64, w1.row_bytes), dtype=torch.uint8)
+    scales = torch.empty(lay.n_gpu_blocks * 64, dtype=torch.float32) if w1.dtype == "fp8" else None
+    W.fill_rows(w1.dtype, rows, scales, W.row_seed(w1, "gpu"))
+    nh = max(lay.n_host_blocks, 1) * 64
+    host = np.zeros((nh, w1.row_bytes), np.uint8)
+    hsc = np.zeros(nh, np.float32) if w1.dtype == "fp8" else None
+    ot = oracle.OracleTiers(
+        page_gpu=lay.page_gpu, page_host=lay.page_host, hot_blocks=lay.hot_blocks,
+        ctx_len=np.full(1, w1.ctx, np.int32), pool_rows=rows.numpy(),
+        pool_scales=None if scales is None else scales.numpy(), host_rows=host, host_scales=hsc,
+        hot_rows=w1.hot_rows, max_ctx=w1.ctx)
+    t_res, n_res, spent = 0.0, 0, 0.0
+    res = gat = gsc = topk = None
+    for s_, topk in enumerate(W.topk_lists(w1)):
+        t0 = time.perf_counter()
+        res, gat, gsc, _, _ = ot.resolve(np.arange(1), topk, nthreads=threads)
+        dt = time.perf_counter() - t0
+        t_res, n_res, spent = t_res + dt, n_res + 1, spent + dt
+        if spent > budget_s / 4 or s_ >= 7:
+            break
+    q = W.make_q(w1, 0).view(torch.int16).numpy().view(np.uint16)
+    n_all = w1.T * w1.H
+    n_rows = 16
+    t0 = time.perf_counter()
+    while True:
+        idx = np.arange(min(n_rows, n_all))
+        sel = np.stack([np.zeros_like(idx), idx // w1.H, idx % w1.H], 1).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.sparse_mla_decode(q, gat, gsc, res, topk, np.full(1, w1.ctx, np.int32), w1.sm_scale,
+                                 sel=sel, nthreads=threads)
+        t_att = time.perf_counter() - t0
+        if t_att > budget_s / 2 or n_rows >= n_all:
+            break
+        n_rows = min(n_all, n_rows * 4)
+    per_req = t_res / n_res
+    per_row = t_att / len(idx)
+    step_s = B * per_req + B * w.T * w.H * per_row
+    return {"value": round(1.0 / step_s, 6), "unit": "decode steps/s", "cores": threads,
+            "kind": "oracle",
+            "sample": (f"{label}: resolve of {n_res} steps and attention of {len(idx)} of its "
+                       f"{n_all} query rows, extrapolated to {B} requests x {w.T * w.H} query "
+                       f"rows per step; {spent + t_att:.1f} s of CPU work")}
 
 
 def run_reference(args):
@@ -700,20 +826,25 @@ def run_reference(args):
     budget = 150.0 / (args.steps + args.warmup)
     _, _, t_res, t_row = smp.step(0, 8)
     n_rows = int(max(1, min(w.T * w.H, (budget - t_res) / max(t_row, 1e-9))))
-    times = []
+    times, walls = [], []
     for s in range(args.warmup + args.steps):
-        e, _, _, _ = smp.step(s, n_rows)
+        e, m, _, _ = smp.step(s, n_rows)
         if s >= args.warmup:
             times.append(e)
+            walls.append(m)
     ms = 1e3 * sum(times) / len(times)
+    wall_ms = 1e3 * sum(walls) / len(walls)
     v = 1e3 / ms
     sample = (f"each step: resolve of 1 of {w.B} requests and attention of {n_rows} of its "
               f"{w.T * w.H} query rows, extrapolated to the full {w.B}-request step")
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 5), "unit": "decode steps/s",
-            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(wall_ms, 3),
+            "ms_per_step_extrapolated": round(ms, 3),
+            "timing": ("ms_per_step is the wall time of the sampled work actually run per step; "
+                       "value is the full step's rate extrapolated from it (ms_per_step_extrapolated)"),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic",
-            "config": {"workload": WORKLOAD_DESC, "global_batch": w.B, "top_k": w.K},
+            "data": "synthetic", "config": run_config(WORKLOAD_DESC, w, ws),
             "cpu_baseline": {"value": round(v, 5), "unit": "decode steps/s", "cores": threads,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(v, 5), "unit": "decode steps/s", "h2d_bytes_per_step": 0,
@@ -731,6 +862,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work spent on the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the other configurations measured after the headline")
     ap.add_argument("--batch", type=int, default=0,
                     help="requests per step (default: the workload's; smaller only for profiling)")
     ap.add_argument("--transitions", action="store_true",
