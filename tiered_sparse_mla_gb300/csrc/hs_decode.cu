@@ -934,43 +934,42 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 }
 
 // Merges the KV-split partials: out = sum_s w_s O_s / sum_s w_s, w_s = exp(lse_s - max).
+// One thread per 8 output columns of a row (64 threads per row): every load
+// of a thread is independent of the others, so the whole merge is about one
+// round trip to memory.
 __global__ void __launch_bounds__(256)
 combine_kernel(const __nv_bfloat16 *__restrict__ ws_o, const float *__restrict__ ws_lse, int nsplit,
                int rows, __nv_bfloat16 *__restrict__ out, float *__restrict__ lse) {
     grid_dep_wait();  // the decode grid's partials are complete
-    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 256 + threadIdx.x;
+    const int row = t >> 6, c8 = (t & 63) * 8;
     if (row >= rows) return;
     float mx = -INFINITY;
     for (int s = 0; s < nsplit; ++s) mx = fmaxf(mx, ws_lse[(size_t)s * rows + row]);
-    float acc[16];
+    float acc[8];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
     float wsum = 0.f;
     if (mx != -INFINITY) {
+#pragma unroll 4
         for (int s = 0; s < nsplit; ++s) {
             const float ls = ws_lse[(size_t)s * rows + row];
-            if (ls == -INFINITY) continue;
-            const float w = __expf(ls - mx);
+            const uint4 u = *reinterpret_cast<const uint4 *>(ws_o + ((size_t)s * rows + row) * 512 + c8);
+            const float w = ls == -INFINITY ? 0.f : __expf(ls - mx);
             wsum += w;
-            const uint2 *src = reinterpret_cast<const uint2 *>(ws_o + ((size_t)s * rows + row) * 512);
+            const uint32_t v[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint2 u = src[lane + 32 * q];  // elements 4 (lane + 32 q) .. + 3
-                acc[4 * q] += w * __uint_as_float(u.x << 16);
-                acc[4 * q + 1] += w * __uint_as_float(u.x & 0xffff0000u);
-                acc[4 * q + 2] += w * __uint_as_float(u.y << 16);
-                acc[4 * q + 3] += w * __uint_as_float(u.y & 0xffff0000u);
+            for (int e = 0; e < 4; ++e) {
+                acc[2 * e] += w * __uint_as_float(v[e] << 16);
+                acc[2 * e + 1] += w * __uint_as_float(v[e] & 0xffff0000u);
             }
         }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    uint2 *dst = reinterpret_cast<uint2 *>(out + (size_t)row * 512);
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-        dst[lane + 32 * q] = make_uint2(pack_bf16(acc[4 * q] * inv, acc[4 * q + 1] * inv),
-                                        pack_bf16(acc[4 * q + 2] * inv, acc[4 * q + 3] * inv));
-    if (lane == 0) lse[row] = wsum > 0.f ? mx + __logf(wsum) : -INFINITY;
+    *reinterpret_cast<uint4 *>(out + (size_t)row * 512 + c8) =
+        make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
+                   pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
+    if (c8 == 0) lse[row] = wsum > 0.f ? mx + __logf(wsum) : -INFINITY;
 }
 
 // ---------------------------------------------------------------- host side
@@ -1197,7 +1196,7 @@ hs_status decode_entry(hs_pool_t pool, int32_t B, int32_t T, int32_t tpl, int32_
     if (pl.nsplit > 1) {
         const int rows = B * pl.M;
         cudaLaunchConfig_t cc = {};
-        cc.gridDim = dim3((rows + 7) / 8, 1, 1);
+        cc.gridDim = dim3((rows + 3) / 4, 1, 1);
         cc.blockDim = dim3(256, 1, 1);
         cc.stream = s;
         cudaLaunchAttribute ca[1];
