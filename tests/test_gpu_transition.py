@@ -19,7 +19,9 @@ def _lib():
 
 class _Full:
     """A fully resident pool (every page on the GPU, no host copies yet) with a
-    host arena of one block per page, and the oracle's own copy of it."""
+    host arena of one block per page, and the oracle's own copy of it. Both
+    host arenas start with the same seeded random bytes (and scales), so that
+    a write into a block that no transition names shows up as a difference."""
 
     def __init__(self, w):
         import oracle
@@ -37,6 +39,13 @@ class _Full:
             self.pool.page_map_range(r, 0, self.page_gpu[r], np.full(P, -1, np.int32))
             self.pool.hot_lease(r, hot[r])
         W.fill_rows(w.dtype, self.pool.gpu_rows(), self.pool.gpu_scales(), W.row_seed(w, "gpu"))
+        rng = np.random.default_rng(W.row_seed(w, "host"))
+        host0 = rng.integers(0, 256, size=(w.B * P * PAGE, w.row_bytes), dtype=np.uint8)
+        self.pool.host_rows()[:] = host0
+        hsc0 = None
+        if fp8:
+            hsc0 = rng.random(w.B * P * PAGE, dtype=np.float32)
+            self.pool.host_scales()[:] = hsc0
         torch.cuda.synchronize()
         sc = self.pool.gpu_scales()
         self.ot = oracle.OracleTiers(
@@ -44,8 +53,7 @@ class _Full:
             hot_blocks=hot, ctx_len=np.full(w.B, w.ctx, np.int32),
             pool_rows=self.pool.gpu_rows().cpu().numpy().copy(),
             pool_scales=None if sc is None else sc.cpu().numpy().copy(),
-            host_rows=np.zeros((w.B * P * PAGE, w.row_bytes), np.uint8),
-            host_scales=np.zeros(w.B * P * PAGE, np.float32) if fp8 else None,
+            host_rows=host0.copy(), host_scales=None if hsc0 is None else hsc0.copy(),
             hot_rows=w.hot_rows, max_ctx=w.ctx)
         dev = "cuda"
         self.req_ids = torch.arange(w.B, dtype=torch.int32, device=dev)
@@ -84,12 +92,11 @@ def test_active_copy_demote_then_resolve(dtype):
     assert f.pool.get_error() == 0
     assert f.ot.active_copy(reqs, pages, hbs) == 0
     f.check_tables()
-    # the copied host blocks (the others hold whatever the arena held before)
-    rows = (hbs[:, None] * PAGE + np.arange(PAGE)).reshape(-1)
-    assert np.array_equal(f.pool.host_rows()[rows], f.ot.host_rows[rows])
+    # the whole host arena: the copied blocks and, untouched, every other one
+    assert np.array_equal(f.pool.host_rows(), f.ot.host_rows)
     if dtype == "fp8":
-        assert np.array_equal(f.pool.host_scales()[rows].view(np.uint32),
-                              f.ot.host_scales[rows].view(np.uint32))
+        assert np.array_equal(f.pool.host_scales().view(np.uint32),
+                              f.ot.host_scales.view(np.uint32))
     # demotion: request 0 to the workload's tail, 1 to nothing, 2 keeps everything
     keep = np.array([w.resident_tail, 0, w.ctx], np.int32)
     freed = torch.full((w.B, w.pages), -7, dtype=torch.int32, device="cuda")
