@@ -477,6 +477,8 @@ def measure(args, name, steps, with_e2e=False):
 # Configurations measured after the headline in the default run (one object
 # per configuration in the same JSON line); the agent mix runs all its steps.
 PER_CONFIG = ["tiny", "hybrid", "noresident", "agent"]
+# the headline workload again with rows read in place by the decode (no gathered buffer)
+PER_CONFIG_VARIANTS = {"resident_in_place": ("resident", {"in_place": True})}
 PER_CONFIG_KEYS = ("value", "unit", "steps", "ms_per_step", "resolved_rows_per_s", "resolve_ms",
                    "decode_ms", "counts_per_step", "roofline", "kernels", "host_link", "clocks",
                    "per_turn_ms", "dtype")
@@ -510,6 +512,14 @@ def run_gpu(args):
             if rank == 0 and ws == 1 and not args.no_cpu_baseline:
                 entry["cpu_baseline"] = cpu_baseline_config(name, wn, args)
             per[name] = entry
+        for key, (name, over) in PER_CONFIG_VARIANTS.items():
+            torch.cuda.empty_cache()
+            sub_args = argparse.Namespace(**{**vars(args), **over})
+            sub, wn = measure(sub_args, name, max(args.steps, 32))
+            entry = {k: sub[k] for k in PER_CONFIG_KEYS if k in sub}
+            entry["workload"] = sub["config"]["workload"]
+            entry["rows"] = sub["config"]["rows"]
+            per[key] = entry
         line["per_config"] = per
     if rank == 0:
         print(json.dumps(line), flush=True)

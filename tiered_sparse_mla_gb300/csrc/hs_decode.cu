@@ -139,6 +139,7 @@ struct DecParams {
     const int32_t *resolved, *topk, *req_ids, *ctx;
     const float *gscale;        // gathered row scales (FP8, gathered rows)
     const float *pool_scales;   // pool row scales (FP8, rows read in place)
+    const uint8_t *pool_rows;   // the pool's rows (rows read in place)
     int zero_row;               // pool row of zeros read for absent entries (in place)
     __nv_bfloat16 *out;
     float *lse, *ws_lse;
@@ -350,9 +351,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         mbar_init(bar(C::B_QREADY), NSTG + NSFT);
         mbar_init(bar(C::B_DRAIN), 1);
         for (int g = 0; g < NG; ++g) {
-            mbar_init(bar(C::B_GFULL + g), FP8 ? NCVT : 1);
+            // TMA loads complete a tile with one arrive and its bytes; rows read
+            // in place arrive once per producer lane (cp.async completion)
+            mbar_init(bar(C::B_GFULL + g), FP8 ? NCVT : (INPLACE ? 32 : 1));
             mbar_init(bar(C::B_GEMPTY + g), 1);
-            mbar_init(bar(C::B_GLANDED + g), 1);
+            mbar_init(bar(C::B_GLANDED + g), INPLACE ? 32 : 1);
             mbar_init(bar(C::B_KVIS + g), 32);
         }
         mbar_init(bar(C::B_SFULL), 1);
@@ -397,18 +400,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             bar(C::B_QFULL));
         }
         grid_dep_wait();
-        constexpr uint32_t ROWB = FP8 ? 64u : 128u;  // smem bytes of one row of one chunk
-        // in place: pool row ids of this lane's four rows, loaded a tile ahead
-        auto row_ids = [&](int i, int (&rid)[4]) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int j = k0 + i * BN + 4 * lane + q;
-                rid[q] = (INPLACE && lane < 16 && i < ntiles && j < k1)
-                             ? p.resolved[(size_t)b * p.K + j] : -1;
-            }
+        // in place: pool row ids of keys lane and lane + 32 of a tile, loaded
+        // a tile ahead (absent entries read the pool's zero row)
+        auto row_ids = [&](int i, int &lo, int &hi) {
+            const int j = k0 + i * BN + lane;
+            lo = (INPLACE && i < ntiles && j < k1) ? p.resolved[(size_t)b * p.K + j] : -1;
+            hi = (INPLACE && i < ntiles && j + 32 < k1) ? p.resolved[(size_t)b * p.K + j + 32] : -1;
         };
-        int rid_next[4];
-        row_ids(0, rid_next);
+        int nxt_lo = -1, nxt_hi = -1;
+        row_ids(0, nxt_lo, nxt_hi);
         int issued = 0;
         bool ok = true;
         for (int i = 0; i < ntiles; ++i) {
@@ -426,17 +426,43 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             const uint32_t done = bar((FP8 ? C::B_GLANDED : C::B_GFULL) + g);
             if (INPLACE) {
-                int rid[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) rid[q] = rid_next[q] >= 0 ? rid_next[q] : p.zero_row;
-                row_ids(i + 1, rid_next);
-                if (lane == 0) mbar_expect_tx(done, NLC * (FP8 ? FCH_BYTES : KCH_BYTES));
-                __syncwarp();
-                if (lane < 16)
-                    for (int lc = 0; lc < NLC; ++lc)
-                        tma_gather4((FP8 ? codes(g, lc) : slot(g, lc)) + 4u * ROWB * lane, &tm_kv,
-                                    64 * (lc < 4 ? 4 * half + lc : 8), rid[0], rid[1], rid[2], rid[3],
-                                    done);
+                // every lane copies 16-byte pieces of the tile's rows from the
+                // pool with cp.async: one instruction covers the value half of
+                // one row (BF16: 32 pieces) or of two (FP8 codes: 16 each), then
+                // the rope chunk of four (BF16) or eight (FP8) rows; BF16
+                // pieces land in the 128-byte-swizzled layout the MMA reads,
+                // FP8 codes packed [chunk][row][64 B] for the converters
+                const int lo = nxt_lo >= 0 ? nxt_lo : p.zero_row;
+                const int hi = nxt_hi >= 0 ? nxt_hi : p.zero_row;
+                row_ids(i + 1, nxt_lo, nxt_hi);
+                constexpr int RB = FP8 ? hs::kDim : 2 * hs::kDim;  // row bytes
+                constexpr int VP = FP8 ? 16 : 32;                  // 16-byte pieces of a value half
+                constexpr int RP = FP8 ? 4 : 8;                    // 16-byte pieces of the rope chunk
+                const uint8_t *pool = p.pool_rows;
+#pragma unroll 4
+                for (int m = 0; m < BN * VP / 32; ++m) {
+                    const int k = m * (32 / VP) + lane / VP, pc = lane % VP;
+                    const int ra = __shfl_sync(0xffffffffu, lo, k & 31);
+                    const int rb2 = __shfl_sync(0xffffffffu, hi, k & 31);
+                    const int r = k < 32 ? ra : rb2;
+                    const uint8_t *src = pool + (size_t)r * RB + half * (RB / 9 * 4) + pc * 16;
+                    const uint32_t dst = FP8 ? codes(g, pc >> 2) + (uint32_t)(k * 64 + (pc & 3) * 16)
+                                             : slot(g, pc >> 3) + (uint32_t)(k * 128 + (((pc & 7) ^ (k & 7)) << 4));
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+                }
+#pragma unroll 4
+                for (int m = 0; m < BN * RP / 32; ++m) {
+                    const int k = m * (32 / RP) + lane / RP, pc = lane % RP;
+                    const int ra = __shfl_sync(0xffffffffu, lo, k & 31);
+                    const int rb2 = __shfl_sync(0xffffffffu, hi, k & 31);
+                    const int r = k < 32 ? ra : rb2;
+                    const uint8_t *src = pool + (size_t)r * RB + (RB / 9 * 8) + pc * 16;
+                    const uint32_t dst = FP8 ? codes(g, 4) + (uint32_t)(k * 64 + pc * 16)
+                                             : slot(g, 4) + (uint32_t)(k * 128 + ((pc ^ (k & 7)) << 4));
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+                }
+                // arrives on the tile's barrier once this lane's copies have landed
+                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(done) : "memory");
             } else if (lane == 0) {
                 // the four value chunks of the tile's 64 rows in one box
                 // ([chunk][row][64]), the rope chunk in another
@@ -494,6 +520,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
                 if (j < ntiles && mbar_test(bar(C::B_GFULL + j % NG), (uint32_t)(j / NG) & 1u) &&
                     (j == 0 || mbar_test(bar(C::B_SFREE), (uint32_t)(j - 1) & 1u))) {
+                    // rows gathered by cp.async were written through the generic
+                    // proxy; the MMA reads shared memory through the async proxy
+                    if (INPLACE) fence_proxy_async();
                     tc_fence_after();
                     const uint64_t b0 = desc_sw128(slot(j % NG, 0), 16, 1024);
                     issue_qk(tmem + TM_S, tmem + TM_Q, (uint32_t)b0, (uint32_t)(b0 >> 32), ID_QK, half);
@@ -1163,6 +1192,7 @@ hs_status decode_entry(hs_pool_t pool, int32_t B, int32_t T, int32_t tpl, int32_
     p.gscale = d_gathered_scale;
     p.pool_scales = pool->d_scales;
     p.zero_row = (int)(pool->cfg.n_gpu_blocks * hs::kPage);
+    p.pool_rows = pool->d_rows;
     p.out = static_cast<__nv_bfloat16 *>(d_out);
     p.lse = d_lse;
     p.ws_o = pl.nsplit > 1 ? static_cast<__nv_bfloat16 *>(d_workspace) : nullptr;
