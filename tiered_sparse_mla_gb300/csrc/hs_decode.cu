@@ -364,9 +364,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             mbar_init(bar(C::B_PFULL + x), NSFT);
             mbar_init(bar(C::B_PVDONE + x), 1);
             mbar_init(bar(C::B_XFULL + x), 1);  // own arm + the peer's bulk copy bytes
-            mbar_init(bar(C::B_XTAKEN + x), 1);
+            mbar_init(bar(C::B_XTAKEN + x), NSFT / 32);  // one arrive per peer softmax warp
             mbar_init(bar(C::B_STAGED + x), NSTG);
-            mbar_init(bar(C::B_READ + x), 1);
+            mbar_init(bar(C::B_READ + x), NSFT / 32);    // one arrive per softmax warp
             mbar_init(bar(C::B_XOUTDONE + x), 1);
         }
         misc[1] = 0;
@@ -778,9 +778,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const int t = vrow ? mg / p.H : 0;  // query token of this row
             const uint32_t peer_xtaken = hs::dsmem_map(smem + C::OFF_BAR + 8 * C::B_XTAKEN, peer);
             float m2 = -INFINITY, l = 0.f;
-            // Every softmax thread runs every half tile and reaches every
-            // named barrier (those are not bounded in time); after a failed
-            // wait the remaining work is skipped.
+            // Every softmax thread runs every half tile; after a failed wait
+            // the remaining work is skipped.
             for (int u = 0; u < nunits; ++u) {
                 const uint32_t x = (uint32_t)(u & 1);
                 const int j = u >> 1, h = u & 1, g = j % NG;
@@ -800,13 +799,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         s[4 * c + 3] = a.w + v.w;
                     }
                 }
-                // X_in[x] and X_out[x] read by every softmax thread: one thread
-                // frees X_out[x] for the stagers and X_in[x] for the peer
-                named_bar_sync(2, NSFT);
-                if (threadIdx.x == 8 * 32) {
-                    // the reads above have returned their values, so an arrive
-                    // without a cluster-scope release (which would wait for a
-                    // cluster-wide fence) is enough to let the peer overwrite
+                // X_in[x] and X_out[x] read by this warp: lane 0 frees them for the
+                // stagers and the peer, one arrive per warp (the reads above have
+                // returned their values, so an arrive without a cluster-scope
+                // release is enough to let the peer overwrite)
+                __syncwarp();
+                if (lane == 0) {
                     mbar_arrive(bar(C::B_READ + x));
                     mbar_arrive_peer(peer_xtaken + 8u * x);
                 }
