@@ -15,16 +15,16 @@
 // The 576-wide rows are nine 64-column chunks: eight value chunks and the rope
 // chunk 8. CTA h (h = 0, 1):
 //   - loads, per 64-key tile, its four value chunks 4h..4h+3 and the rope
-//     chunk (40 KB of BF16 rows, 20 KB of FP8 codes);
+//     chunk (40 KB of BF16 rows, 20 KB of FP8 codes; rows read in place from
+//     the pool bring only the half of the rope chunk this CTA uses);
 //   - holds Q in tensor memory for those value chunks and for its half of the
 //     rope chunk (columns 32h..32h+31 of it), so that each CTA computes S over
 //     288 of the 576 depth columns;
-//   - sends its partial S, in f32 and already multiplied by sm_scale*log2(e)
-//     (times the row scale for FP8), straight from registers to the peer's
-//     shared memory (each warp's stores, then one release-arrive per warp on
-//     the peer's barrier) and adds the peer's partial; f32 addition is
-//     commutative, so both CTAs hold bit-identical S and take identical
-//     softmax decisions;
+//   - writes its partial S of each half tile (32 keys), in f32 and already
+//     multiplied by sm_scale*log2(e) (times the row scale for FP8), to shared
+//     memory, sends it to the peer with one 16 KB bulk copy, and adds the
+//     peer's partial; f32 addition is commutative, so both CTAs hold
+//     bit-identical S and take identical softmax decisions;
 //   - accumulates O for output columns [256h, 256h + 256) (its value chunks)
 //     with P in tensor memory.
 // FP8 rows: the codes are turned into BF16 exactly (each code's bits placed as
@@ -32,31 +32,38 @@
 // scale multiplies the scores of that key in f32, and its probability before
 // P is rounded to BF16 (the sum of probabilities stays unscaled). So Q stays
 // BF16 on both paths and no operand is rounded beyond BF16.
-// Roles inside a CTA (256 threads for BF16 rows, 384 for FP8):
-//   warp 0      TMA producer: Q once, into the space of tile groups 2-3 (their
-//               first loads wait until Q has moved to TMEM), then per tile one
-//               box of the four value chunks and one of the rope chunk (or, in
-//               place, four-row gathers from the pool);
+// Roles inside a CTA (384 threads):
+//   warp 0      producer: Q once by TMA, into the space of tile groups 2-3
+//               (their first loads wait until Q has moved to TMEM), then per
+//               tile one TMA box of the four value chunks and one of the rope
+//               chunk; rows read in place are copied from the pool in 16-byte
+//               cp.async pieces (BF16: keys 0-31 of each tile, FP8: all 64);
 //   warp 1      MMA issuer (one thread): S_j = Q K_j^T into the TMEM S buffer
-//               once tile j is ready and S_{j-1} has been read; O += P_i V_i
-//               (V read from the same smem chunks as K through an MN-major
-//               descriptor) once P_i is written; PV first when both can go;
+//               once tile j is ready and S_{j-1} has been read; O += P_u V_u
+//               per half tile u (V read from the same smem chunks as K through
+//               an MN-major descriptor) once P_u is written; PV first when both
+//               can go;
 //   warp 2      per tile: the lowest query token that sees each key, and for
 //               FP8 the key's row scale, into shared rings, so that no row
-//               thread waits on a global load;
-//   warp 3      idle;
-//   warps 4-7   row threads, one per query row (TMEM lane): read S_{j+1},
-//               free it for the next QK and send the partial to the peer, then
-//               the softmax of tile j (add the peer's partial, mask, online
-//               softmax with a conditional rescale, P to TMEM), epilogue. The
-//               send of tile j+1 goes out before the softmax of tile j, so the
-//               exchange overlaps the softmax;
-//   warps 8-11  FP8 only: convert each landed tile of codes to BF16 in place.
+//               thread waits on a global load; BF16 rows read in place: the
+//               copies of keys 32-63;
+//   warp 3      courier (one thread): the bulk copies of the partial S to the
+//               peer, each once the peer has read the half tile sent two
+//               before into the same buffer;
+//   warps 4-7   stagers, one thread per query row (TMEM lane): read S_j, free
+//               it for the next QK, scale it and write both halves to the
+//               outgoing buffers; FP8: also convert each landed tile of codes
+//               to BF16 in place, two tiles ahead of its QK;
+//   warps 8-11  softmax, one thread per query row, per half tile: add the two
+//               partials, mask, online softmax with a conditional rescale, P
+//               to TMEM; then the epilogue (O / l through shared memory and
+//               TMA stores).
 // TMEM (512 columns): O half 256 | S 64 | P 32 | Q 144.
 // Every mbarrier wait is bounded in time; on expiry the kernel sets
 // HS_DEVERR_TIMEOUT, drains its own copies and MMAs and returns. Roles hand
-// over through mbarriers only, so one that gives up leaves no other waiting
-// on a hardware barrier.
+// over through mbarriers, so one that gives up leaves no other waiting on a
+// hardware barrier (the FP8 stagers' named barrier is reached by all four
+// stager warps on every path).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -231,17 +238,6 @@ __device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int
         : "memory");
 }
 
-// Four rows (r0..r3) of a 2-D tensor map, each one box wide starting at
-// column x, to consecutive box-sized places at dst.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int x, int r0, int r1,
-                                            int r2, int r3, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-        : "memory");
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
@@ -345,6 +341,38 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         misc[1] = 1;
         atomicOr(p.err, HS_DEVERR_TIMEOUT);
     };
+    // Rows read in place: keys kb..kb + 31 of a tile (lane i holds the pool row
+    // of key kb + i in `rows`) copied from the pool in 16-byte pieces with
+    // cp.async, the value half of one row (BF16) or of two (FP8 codes) per
+    // instruction, then the half of the rope chunk this CTA's QK reads. BF16
+    // pieces land in the 128-byte-swizzled layout the MMA reads, FP8 codes
+    // packed [chunk][row][64 B] for the converters. Called by a whole warp.
+    auto gather_keys = [&](int g, int rows, int kb) {
+        constexpr int RB = FP8 ? hs::kDim : 2 * hs::kDim;  // row bytes
+        constexpr int VP = FP8 ? 16 : 32;                  // 16-byte pieces of a value half
+        constexpr int RH = FP8 ? 2 : 4;                    // 16-byte pieces of half the rope chunk
+        const uint8_t *pool = p.pool_rows;
+#pragma unroll 4
+        for (int m = 0; m < VP; ++m) {
+            const int kk = m * (32 / VP) + lane / VP, pc = lane % VP;
+            const int r = __shfl_sync(0xffffffffu, rows, kk);
+            const int k = kb + kk;
+            const uint8_t *src = pool + (size_t)r * RB + half * (RB / 9 * 4) + pc * 16;
+            const uint32_t dst = FP8 ? codes(g, pc >> 2) + (uint32_t)(k * 64 + (pc & 3) * 16)
+                                     : slot(g, pc >> 3) + (uint32_t)(k * 128 + (((pc & 7) ^ (k & 7)) << 4));
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+        }
+#pragma unroll
+        for (int m = 0; m < RH; ++m) {
+            const int kk = m * (32 / RH) + lane / RH, pc = RH * half + lane % RH;
+            const int r = __shfl_sync(0xffffffffu, rows, kk);
+            const int k = kb + kk;
+            const uint8_t *src = pool + (size_t)r * RB + (RB / 9 * 8) + pc * 16;
+            const uint32_t dst = FP8 ? codes(g, 4) + (uint32_t)(k * 64 + pc * 16)
+                                     : slot(g, 4) + (uint32_t)(k * 128 + ((pc ^ (k & 7)) << 4));
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+        }
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::B_QFULL), 1);
@@ -353,7 +381,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         for (int g = 0; g < NG; ++g) {
             // TMA loads complete a tile with one arrive and its bytes; rows read
             // in place arrive once per producer lane (cp.async completion)
-            mbar_init(bar(C::B_GFULL + g), FP8 ? NCVT : (INPLACE ? 32 : 1));
+            mbar_init(bar(C::B_GFULL + g), FP8 ? NCVT : (INPLACE ? 64 : 1));
             mbar_init(bar(C::B_GEMPTY + g), 1);
             mbar_init(bar(C::B_GLANDED + g), INPLACE ? 32 : 1);
             mbar_init(bar(C::B_KVIS + g), 32);
@@ -375,8 +403,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (warp == 1) tmem_alloc(base + C::OFF_MISC, TMEM_COLS);
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tm_q);
-        prefetch_tmap(&tm_kv);
-        prefetch_tmap(&tm_kr);
+        if (!INPLACE) {
+            prefetch_tmap(&tm_kv);
+            prefetch_tmap(&tm_kr);
+        }
         prefetch_tmap(&tm_o);
     }
     tc_fence_before();
@@ -392,7 +422,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // ------------------------------------------------------------ producer
         // Lane 0 loads Q and takes each slot; a tile read from the gathered
         // buffer is two boxes (lane 0), a tile read in place from the pool is
-        // 16 four-row gathers per chunk, one per lane 0..15.
+        // copied by all 32 lanes with cp.async.
         if (lane == 0) {
             mbar_expect_tx(bar(C::B_QFULL), NQC * QCH_BYTES);
             for (int c = 0; c < NQC; ++c)
@@ -400,12 +430,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             bar(C::B_QFULL));
         }
         grid_dep_wait();
-        // in place: pool row ids of keys lane and lane + 32 of a tile, loaded
-        // a tile ahead (absent entries read the pool's zero row)
+        // in place: pool row id of key lane of a tile, loaded a tile ahead
+        // (absent entries read the pool's zero row)
         auto row_ids = [&](int i, int &lo, int &hi) {
             const int j = k0 + i * BN + lane;
             lo = (INPLACE && i < ntiles && j < k1) ? p.resolved[(size_t)b * p.K + j] : -1;
-            hi = (INPLACE && i < ntiles && j + 32 < k1) ? p.resolved[(size_t)b * p.K + j + 32] : -1;
+            hi = (FP8 && INPLACE && i < ntiles && j + 32 < k1) ? p.resolved[(size_t)b * p.K + j + 32] : -1;
         };
         int nxt_lo = -1, nxt_hi = -1;
         row_ids(0, nxt_lo, nxt_hi);
@@ -426,41 +456,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             const uint32_t done = bar((FP8 ? C::B_GLANDED : C::B_GFULL) + g);
             if (INPLACE) {
-                // every lane copies 16-byte pieces of the tile's rows from the
-                // pool with cp.async: one instruction covers the value half of
-                // one row (BF16: 32 pieces) or of two (FP8 codes: 16 each), then
-                // the rope chunk of four (BF16) or eight (FP8) rows; BF16
-                // pieces land in the 128-byte-swizzled layout the MMA reads,
-                // FP8 codes packed [chunk][row][64 B] for the converters
+                // BF16 rows: keys 0-31 here, keys 32-63 by the key-visibility
+                // warp; FP8 codes: all 64 keys here
                 const int lo = nxt_lo >= 0 ? nxt_lo : p.zero_row;
                 const int hi = nxt_hi >= 0 ? nxt_hi : p.zero_row;
                 row_ids(i + 1, nxt_lo, nxt_hi);
-                constexpr int RB = FP8 ? hs::kDim : 2 * hs::kDim;  // row bytes
-                constexpr int VP = FP8 ? 16 : 32;                  // 16-byte pieces of a value half
-                constexpr int RP = FP8 ? 4 : 8;                    // 16-byte pieces of the rope chunk
-                const uint8_t *pool = p.pool_rows;
-#pragma unroll 4
-                for (int m = 0; m < BN * VP / 32; ++m) {
-                    const int k = m * (32 / VP) + lane / VP, pc = lane % VP;
-                    const int ra = __shfl_sync(0xffffffffu, lo, k & 31);
-                    const int rb2 = __shfl_sync(0xffffffffu, hi, k & 31);
-                    const int r = k < 32 ? ra : rb2;
-                    const uint8_t *src = pool + (size_t)r * RB + half * (RB / 9 * 4) + pc * 16;
-                    const uint32_t dst = FP8 ? codes(g, pc >> 2) + (uint32_t)(k * 64 + (pc & 3) * 16)
-                                             : slot(g, pc >> 3) + (uint32_t)(k * 128 + (((pc & 7) ^ (k & 7)) << 4));
-                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-                }
-#pragma unroll 4
-                for (int m = 0; m < BN * RP / 32; ++m) {
-                    const int k = m * (32 / RP) + lane / RP, pc = lane % RP;
-                    const int ra = __shfl_sync(0xffffffffu, lo, k & 31);
-                    const int rb2 = __shfl_sync(0xffffffffu, hi, k & 31);
-                    const int r = k < 32 ? ra : rb2;
-                    const uint8_t *src = pool + (size_t)r * RB + (RB / 9 * 8) + pc * 16;
-                    const uint32_t dst = FP8 ? codes(g, 4) + (uint32_t)(k * 64 + pc * 16)
-                                             : slot(g, 4) + (uint32_t)(k * 128 + ((pc ^ (k & 7)) << 4));
-                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-                }
+                gather_keys(g, lo, 0);
+                if (FP8) gather_keys(g, hi, 32);
                 // arrives on the tile's barrier once this lane's copies have landed
                 asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(done) : "memory");
             } else if (lane == 0) {
@@ -564,7 +566,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const uint32_t ph = (uint32_t)(i / NG) & 1u;
             // the slot's previous tile is finished (its stagers and softmax read these rings)
             if (ok) ok = mbar_wait(bar(C::B_GEMPTY + g), ph ^ 1u) && !misc[1];
-            int dm[2] = {0, 0};
+            int dm[2] = {0, 0}, rr[2] = {-1, -1};
 #pragma unroll
             for (int h = 0; h < 2; ++h) {  // keys lane and lane + 32; loads issued together
                 const int j = k0 + i * BN + lane + 32 * h;
@@ -575,6 +577,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 d = d < 0 ? 0 : (d > p.T ? p.T : d);
                 const int v = res >= 0 ? (int)d : p.T;
                 dm[h] = v;
+                rr[h] = res;
                 if (ok) {
                     kvis[g * BN + lane + 32 * h] = (int16_t)v;
                     if (FP8) {
@@ -582,6 +585,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         if (res >= 0) sc = INPLACE ? p.pool_scales[res] : gs[j];
                         ksc[g * BN + lane + 32 * h] = sc;
                     }
+                }
+            }
+            if (INPLACE && !FP8) {
+                // keys 32-63 of the tile from the pool (keys 0-31: the producer);
+                // tile groups 2-3 hold the staged Q until it has moved to TMEM
+                if (ok && i == 2) ok = mbar_wait(bar(C::B_QREADY), 0);
+                if (__all_sync(0xffffffffu, ok)) {
+                    gather_keys(g, rr[1] >= 0 ? rr[1] : p.zero_row, 32);
+                    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(
+                                     bar((FP8 ? C::B_GLANDED : C::B_GFULL) + g))
+                                 : "memory");
                 }
             }
             // the largest d of each half tile: rows with t >= it skip the mask
@@ -593,6 +607,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             mbar_arrive(bar(C::B_KVIS + g));
         }
+        if (INPLACE && !FP8) asm volatile("cp.async.wait_all;" ::: "memory");  // own copies landed before exit
         if (!ok) fail();
     } else if (warp == 3) {
         // ------------------------------------------------------------ courier
@@ -1163,13 +1178,10 @@ hs_status decode_entry(hs_pool_t pool, int32_t B, int32_t T, int32_t tpl, int32_
         return HS_ERR_CUDA;
     bool ok_k;
     if (inplace) {
-        // the pool as [rows][576] with one-row boxes, for four-row gathers
-        const uint64_t nrows = (uint64_t)(pool->cfg.n_gpu_blocks + 1) * hs::kPage;
-        ok_k = fp8 ? make_map(&tkv, CU_TENSOR_MAP_DATA_TYPE_UINT8, pool->d_rows, hs::kDim, nrows, 1,
-                              hs::kDim, 64, 1, CU_TENSOR_MAP_SWIZZLE_NONE, 2)
-                   : make_map(&tkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pool->d_rows, hs::kDim, nrows,
-                              1, 2 * hs::kDim, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B, 2);
-        tkr = tkv;
+        // not read: rows read in place are copied from the pool with cp.async
+        tkv = tq;
+        tkr = tq;
+        ok_k = true;
     } else {
         // [B][K][9 chunks][64] viewed as (column, row, chunk, request): one box
         // brings four value chunks of 64 rows (chunk-major in shared memory),
