@@ -68,9 +68,10 @@ def _peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def _traffic(kernel: str, src: str):
+def _traffic(kernel: str, src: str, in_place: bool):
     """DRAM bytes per launch from the committed ncu summary, if the kernel's
-    source is unchanged since the capture (else None)."""
+    source is unchanged since the capture and the rows reached attention the
+    same way (in place or gathered) as in the capture (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -78,7 +79,9 @@ def _traffic(kernel: str, src: str):
     if not d:
         return None
     sha = hashlib.sha256(open(os.path.join(ROOT, src), "rb").read()).hexdigest()[:16]
-    return d["dram_bytes_per_launch"] if d.get("source_sha") == sha else None
+    if d.get("source_sha") != sha or d.get("in_place") != in_place:
+        return None
+    return d["dram_bytes_per_launch"]
 
 
 class ClockSampler:
@@ -191,6 +194,12 @@ DESCS = {
               "full/hybrid/none from a seeded pressure schedule"),
 }
 DEFAULT_STEPS = {"resident": 2000, "tiny": 2000, "hybrid": 512, "noresident": 256, "agent": 715}
+# How each workload's rows reach attention by default: read in place from the
+# pool (no gathered buffer) where that gives the shorter step on a GB300,
+# gathered by the resolve elsewhere (measured: resident 17.6K steps/s in place
+# against 14.0K gathered; the FP8 workloads equal or faster gathered)
+DEFAULT_IN_PLACE = {"resident": True, "tiny": False, "hybrid": False, "noresident": False,
+                    "agent": False}
 
 
 def _link_peak_gbs(to_host: bool = False):
@@ -391,13 +400,16 @@ def measure(args, name, steps, with_e2e=False):
     kernels = {
         "resolve": {"ms": res_ms, "achieved": r_hbm / (res_ms * 1e-3) / 1e9, "unit": "GB/s",
                     "peak": hbm_peak, "bound": "hbm", "bytes_per_launch": r_hbm,
-                    "traffic": _traffic("resolve", "tiered_sparse_mla_gb300/csrc/hs_resolve.cu")},
+                    "traffic": _traffic("resolve", "tiered_sparse_mla_gb300/csrc/hs_resolve.cu",
+                                        args.in_place)},
         "decode": {"ms": dec_ms, "achieved": d_bytes / (dec_ms * 1e-3) / 1e9, "unit": "GB/s",
                    "peak": hbm_peak, "bound": "hbm", "bytes_per_launch": d_bytes,
                    "tflops": flops / (dec_ms * 1e-3) / 1e12,
-                   "traffic": _traffic("decode", "tiered_sparse_mla_gb300/csrc/hs_decode.cu")},
+                   "traffic": _traffic("decode", "tiered_sparse_mla_gb300/csrc/hs_decode.cu",
+                                       args.in_place)},
     }
-    if name != WORKLOAD or w.B != W.WORKLOADS[WORKLOAD].B or L > 1 or args.in_place or per_token:
+    if name != WORKLOAD or w.B != W.WORKLOADS[WORKLOAD].B or L > 1 or per_token \
+            or args.in_place != DEFAULT_IN_PLACE[WORKLOAD]:
         kernels["resolve"]["traffic"] = kernels["decode"]["traffic"] = None  # captured on another workload
     # the decode's roofline time is max(bytes / BW, flops / tensor peak)
     t_bytes = d_bytes / (hbm_peak * 1e9)
@@ -477,8 +489,8 @@ def measure(args, name, steps, with_e2e=False):
 # Configurations measured after the headline in the default run (one object
 # per configuration in the same JSON line); the agent mix runs all its steps.
 PER_CONFIG = ["tiny", "hybrid", "noresident", "agent"]
-# the headline workload again with rows read in place by the decode (no gathered buffer)
-PER_CONFIG_VARIANTS = {"resident_in_place": ("resident", {"in_place": True})}
+# the headline workload again with its rows gathered by the resolve
+PER_CONFIG_VARIANTS = {"resident_gathered": ("resident", {"in_place": False})}
 PER_CONFIG_KEYS = ("value", "unit", "steps", "ms_per_step", "resolved_rows_per_s", "resolve_ms",
                    "decode_ms", "counts_per_step", "roofline", "kernels", "host_link", "clocks",
                    "per_turn_ms", "dtype")
@@ -494,8 +506,8 @@ def run_gpu(args):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     import __graft_entry__ as g
     g.build()
-    plain = args.layers <= 1 and not args.in_place and not args.per_token and not args.batch \
-        and not args.ctx
+    plain = args.layers <= 1 and args.in_place == DEFAULT_IN_PLACE[args.workload] \
+        and not args.per_token and not args.batch and not args.ctx
     headline = args.workload == WORKLOAD and plain
     line, w = measure(args, args.workload, args.steps, with_e2e=headline or args.workload == WORKLOAD)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and args.workload == WORKLOAD \
@@ -506,9 +518,11 @@ def run_gpu(args):
         for name in PER_CONFIG:
             n_steps = DEFAULT_STEPS[name] if name == "agent" else max(args.steps, 32)
             torch.cuda.empty_cache()
-            sub, wn = measure(args, name, n_steps)
+            sub_args = argparse.Namespace(**{**vars(args), "in_place": DEFAULT_IN_PLACE[name]})
+            sub, wn = measure(sub_args, name, n_steps)
             entry = {k: sub[k] for k in PER_CONFIG_KEYS if k in sub}
             entry["workload"] = sub["config"]["workload"]
+            entry["rows"] = sub["config"]["rows"]
             if rank == 0 and ws == 1 and not args.no_cpu_baseline:
                 entry["cpu_baseline"] = cpu_baseline_config(name, wn, args)
             per[name] = entry
@@ -854,7 +868,8 @@ def run_reference(args):
             "timing": ("ms_per_step is the wall time of the sampled work actually run per step; "
                        "value is the full step's rate extrapolated from it (ms_per_step_extrapolated)"),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": run_config(WORKLOAD_DESC, w, ws),
+            "data": "synthetic",
+            "config": run_config(WORKLOAD_DESC, w, ws, 1, DEFAULT_IN_PLACE[WORKLOAD]),
             "cpu_baseline": {"value": round(v, 5), "unit": "decode steps/s", "cores": threads,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(v, 5), "unit": "decode steps/s", "h2d_bytes_per_step": 0,
@@ -883,7 +898,11 @@ def main():
     ap.add_argument("--per-token", action="store_true",
                     help="one top-K list per query token: union resolve + per-token decode")
     ap.add_argument("--in-place", action="store_true",
-                    help="attention reads rows from the pool by id; no gathered buffer")
+                    help="attention reads rows from the pool by id; no gathered buffer "
+                         "(the resident workload's default)")
+    ap.add_argument("--gathered", action="store_true",
+                    help="the resolve gathers the rows into a buffer that attention reads "
+                         "(the other workloads' default)")
     ap.add_argument("--ctx", type=int, default=0,
                     help="override the context length (profiling captures only)")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(DESCS),
@@ -892,6 +911,9 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     args.steps = args.steps or DEFAULT_STEPS[args.workload]
+    if args.in_place and args.gathered:
+        ap.error("--in-place and --gathered exclude each other")
+    args.in_place = args.in_place or (not args.gathered and DEFAULT_IN_PLACE[args.workload])
     if args.impl == "reference":
         run_reference(args)
     elif args.transitions:

@@ -64,10 +64,13 @@ def test_per_token_counts_distinct_rows_once(bench):
 
 def test_traffic_record_follows_the_source_hash(bench):
     """A recorded DRAM figure is reported only while the kernel's source is the
-    one it was captured from."""
+    one it was captured from, and only for the way rows reached attention in
+    the capture (in place or gathered)."""
     rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
     for k in ("resolve", "decode"):
         src = rec[k]["source"]
         sha = hashlib.sha256(open(os.path.join(ROOT, src), "rb").read()).hexdigest()[:16]
-        got = bench._traffic(k, src)
+        mode = rec[k]["in_place"]
+        got = bench._traffic(k, src, mode)
         assert got == (rec[k]["dram_bytes_per_launch"] if sha == rec[k]["source_sha"] else None)
+        assert bench._traffic(k, src, not mode) is None

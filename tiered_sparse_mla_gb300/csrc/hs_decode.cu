@@ -37,7 +37,7 @@
 //               (their first loads wait until Q has moved to TMEM), then per
 //               tile one TMA box of the four value chunks and one of the rope
 //               chunk; rows read in place are copied from the pool in 16-byte
-//               cp.async pieces (BF16: keys 0-31 of each tile, FP8: all 64);
+//               cp.async pieces (keys 0-31 of each tile);
 //   warp 1      MMA issuer (one thread): S_j = Q K_j^T into the TMEM S buffer
 //               once tile j is ready and S_{j-1} has been read; O += P_u V_u
 //               per half tile u (V read from the same smem chunks as K through
@@ -45,8 +45,9 @@
 //               can go;
 //   warp 2      per tile: the lowest query token that sees each key, and for
 //               FP8 the key's row scale, into shared rings, so that no row
-//               thread waits on a global load; BF16 rows read in place: the
-//               copies of keys 32-63;
+//               thread waits on a global load; rows read in place: the
+//               copies of keys 32-63, with the ids and scales loaded a tile
+//               ahead;
 //   warp 3      courier (one thread): the bulk copies of the partial S to the
 //               peer, each once the peer has read the half tile sent two
 //               before into the same buffer;
@@ -383,7 +384,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // in place arrive once per producer lane (cp.async completion)
             mbar_init(bar(C::B_GFULL + g), FP8 ? NCVT : (INPLACE ? 64 : 1));
             mbar_init(bar(C::B_GEMPTY + g), 1);
-            mbar_init(bar(C::B_GLANDED + g), INPLACE ? 32 : 1);
+            mbar_init(bar(C::B_GLANDED + g), INPLACE ? 64 : 1);
             mbar_init(bar(C::B_KVIS + g), 32);
         }
         mbar_init(bar(C::B_SFULL), 1);
@@ -432,13 +433,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         grid_dep_wait();
         // in place: pool row id of key lane of a tile, loaded a tile ahead
         // (absent entries read the pool's zero row)
-        auto row_ids = [&](int i, int &lo, int &hi) {
+        auto row_id = [&](int i) {
             const int j = k0 + i * BN + lane;
-            lo = (INPLACE && i < ntiles && j < k1) ? p.resolved[(size_t)b * p.K + j] : -1;
-            hi = (FP8 && INPLACE && i < ntiles && j + 32 < k1) ? p.resolved[(size_t)b * p.K + j + 32] : -1;
+            return (INPLACE && i < ntiles && j < k1) ? p.resolved[(size_t)b * p.K + j] : -1;
         };
-        int nxt_lo = -1, nxt_hi = -1;
-        row_ids(0, nxt_lo, nxt_hi);
+        int nxt_lo = row_id(0);
         int issued = 0;
         bool ok = true;
         for (int i = 0; i < ntiles; ++i) {
@@ -456,13 +455,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             const uint32_t done = bar((FP8 ? C::B_GLANDED : C::B_GFULL) + g);
             if (INPLACE) {
-                // BF16 rows: keys 0-31 here, keys 32-63 by the key-visibility
-                // warp; FP8 codes: all 64 keys here
+                // keys 0-31 here, keys 32-63 by the key-visibility warp
                 const int lo = nxt_lo >= 0 ? nxt_lo : p.zero_row;
-                const int hi = nxt_hi >= 0 ? nxt_hi : p.zero_row;
-                row_ids(i + 1, nxt_lo, nxt_hi);
+                nxt_lo = row_id(i + 1);
                 gather_keys(g, lo, 0);
-                if (FP8) gather_keys(g, hi, 32);
                 // arrives on the tile's barrier once this lane's copies have landed
                 asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(done) : "memory");
             } else if (lane == 0) {
@@ -560,34 +556,60 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const float *gs = (FP8 && !INPLACE) ? p.gscale + (size_t)b * p.K : nullptr;
         int16_t *kvis = reinterpret_cast<int16_t *>(smem + C::OFF_KVIS);
         float *ksc = reinterpret_cast<float *>(smem + C::OFF_KSC);
+        // Rows read in place: the row ids and positions of tile i + 1, and its
+        // row scales (FP8, found through the row ids), are loaded while tile i
+        // is written and copied, so no global-load latency sits between two
+        // tiles of this warp. From the gathered buffer each tile's entries are
+        // loaded after its slot is free (measured faster there).
+        auto load_ids = [&](int i, int (&res)[2], int (&top)[2]) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // keys lane and lane + 32
+                const int j = k0 + i * BN + lane + 32 * h;
+                const bool in = i < ntiles && j < k1;
+                res[h] = in ? res_b[j] : -1;
+                top[h] = in ? top_b[j] : 0;
+            }
+        };
+        auto load_scales = [&](int i, const int (&res)[2], float (&sc)[2]) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                sc[h] = 0.f;
+                if (FP8 && res[h] >= 0) sc[h] = INPLACE ? p.pool_scales[res[h]] : gs[k0 + i * BN + lane + 32 * h];
+            }
+        };
+        int nres[2] = {-1, -1}, ntop[2] = {0, 0};
+        float nsc[2] = {0.f, 0.f};
+        if (INPLACE) {
+            load_ids(0, nres, ntop);
+            load_scales(0, nres, nsc);
+        }
         bool ok = true;
         for (int i = 0; i < ntiles; ++i) {
             const int g = i % NG;
             const uint32_t ph = (uint32_t)(i / NG) & 1u;
+            int cres[2] = {nres[0], nres[1]}, ctop[2] = {ntop[0], ntop[1]};
+            float csc[2] = {nsc[0], nsc[1]};
+            if (INPLACE) load_ids(i + 1, nres, ntop);
             // the slot's previous tile is finished (its stagers and softmax read these rings)
             if (ok) ok = mbar_wait(bar(C::B_GEMPTY + g), ph ^ 1u) && !misc[1];
+            if (!INPLACE) {
+                load_ids(i, cres, ctop);
+                load_scales(i, cres, csc);
+            }
             int dm[2] = {0, 0}, rr[2] = {-1, -1};
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {  // keys lane and lane + 32; loads issued together
-                const int j = k0 + i * BN + lane + 32 * h;
-                const bool in = j < k1;
-                const int res = in ? res_b[j] : -1;
-                const int top = in ? top_b[j] : 0;
-                long long d = (long long)top - first;
+            for (int h = 0; h < 2; ++h) {
+                long long d = (long long)ctop[h] - first;
                 d = d < 0 ? 0 : (d > p.T ? p.T : d);
-                const int v = res >= 0 ? (int)d : p.T;
+                const int v = cres[h] >= 0 ? (int)d : p.T;
                 dm[h] = v;
-                rr[h] = res;
+                rr[h] = cres[h];
                 if (ok) {
                     kvis[g * BN + lane + 32 * h] = (int16_t)v;
-                    if (FP8) {
-                        float sc = 0.f;
-                        if (res >= 0) sc = INPLACE ? p.pool_scales[res] : gs[j];
-                        ksc[g * BN + lane + 32 * h] = sc;
-                    }
+                    if (FP8) ksc[g * BN + lane + 32 * h] = csc[h];
                 }
             }
-            if (INPLACE && !FP8) {
+            if (INPLACE) {
                 // keys 32-63 of the tile from the pool (keys 0-31: the producer);
                 // tile groups 2-3 hold the staged Q until it has moved to TMEM
                 if (ok && i == 2) ok = mbar_wait(bar(C::B_QREADY), 0);
@@ -606,8 +628,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 tdmax[2 * g + 1] = d1;
             }
             mbar_arrive(bar(C::B_KVIS + g));
+            if (INPLACE && FP8) load_scales(i + 1, nres, nsc);
         }
-        if (INPLACE && !FP8) asm volatile("cp.async.wait_all;" ::: "memory");  // own copies landed before exit
+        if (INPLACE) asm volatile("cp.async.wait_all;" ::: "memory");  // own copies landed before exit
         if (!ok) fail();
     } else if (warp == 3) {
         // ------------------------------------------------------------ courier
