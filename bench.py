@@ -22,6 +22,7 @@ import json
 import math
 import os
 import statistics
+import select
 import subprocess
 import sys
 import time
@@ -96,6 +97,7 @@ class ClockSampler:
         self.p = None
 
     def __enter__(self):
+        self.first = ""
         try:
             self.p = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
@@ -103,17 +105,24 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.p = None
+        if self.p is not None:
+            # the sampler's start-up (its own GPU queries) before the timed
+            # steps, not inside them: wait for its first sample (2 s at most)
+            ready, _, _ = select.select([self.p.stdout], [], [], 2.0)
+            if ready:
+                self.first = self.p.stdout.readline()
         return self
 
     def __exit__(self, *a):
-        self.out = ""
+        self.out = self.first
         if self.p is not None:
             self.p.terminate()
             try:
-                self.out, _ = self.p.communicate(timeout=5)
+                rest, _ = self.p.communicate(timeout=5)
             except subprocess.TimeoutExpired:
                 self.p.kill()
-                self.out, _ = self.p.communicate()
+                rest, _ = self.p.communicate()
+            self.out += rest or ""
 
     def summary(self):
         sm, mx, reasons = [], None, set()
@@ -321,7 +330,7 @@ def measure(args, name, steps, with_e2e=False):
         else:
             gw.pool.resolve_topk(gw.req_ids, t, gw.resolved, gw.gathered, gw.gscale, gw.counts,
                                  stream)
-        if ev is not None:
+        if ev is not None and ev[1] is not None:
             ev[1].record(stream)
         if L > 1:
             for l, x in enumerate(gws):  # the layers' queries: the step's q, reused
@@ -344,46 +353,60 @@ def measure(args, name, steps, with_e2e=False):
             step(s)
     torch.cuda.synchronize()
     assert all(x.pool.get_error() == 0 for x in gws)
-    # timed steps start from the beginning of the step list and its initial state
-    for x, sn in zip(gws, snaps):
-        x.pool.restore(sn)
-    if agent:
-        gw.apply(plan[0])
+    # Timed steps start from the beginning of the step list and its initial
+    # state (restored by each pass).
+    # Pass 1 (the timed region of the line): each step timed from before the
+    # resolve to after the decode, nothing recorded between the two kernels,
+    # so the decode may launch while the resolve runs as it does in use.
+    # Pass 2: the same steps from the same state with an event between the
+    # kernels, for the per-kernel times (that event keeps the decode from
+    # launching early, so pass 2's steps are a few microseconds longer).
+    def run_pass(split):
+        evs = [[torch.cuda.Event(enable_timing=True),
+                torch.cuda.Event(enable_timing=True) if split else None,
+                torch.cuda.Event(enable_timing=True)] for _ in range(steps)]
+        counts_acc = torch.zeros(3, dtype=torch.int64, device="cuda")
+        retagged = torch.zeros((), dtype=torch.int64, device="cuda")
+        for x, sn in zip(gws, snaps):
+            x.pool.restore(sn)
+        if agent:
+            gw.apply(plan[0])
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with ClockSampler(local) as clk, torch.cuda.stream(stream):
+            torch.cuda.nvtx.range_push("timed_region" if not split else "kernel_split")
+            for s in range(steps):
+                if s > 0:
+                    prepare(s)
+                if per_token:
+                    tag_prev.copy_(slot_tag)
+                l2_flush()
+                step(s, evs[s])
+                counts_acc += cnt_all.sum((0, 1)) if L > 1 else gw.counts.sum(0)
+                if per_token:
+                    retagged += (slot_tag != tag_prev).sum()
+            torch.cuda.nvtx.range_pop()
+            torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        if ws > 1:
+            dist.barrier()
+        assert gw.pool.get_error() == 0
+        return evs, counts_acc, retagged, clk, wall
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
-    counts_acc = torch.zeros(3, dtype=torch.int64, device="cuda")
     # distinct placed misses: each takes one slot and retags it (outside the events)
     slot_tag = gw.pool.tables()["slot_tag"]
     tag_prev = torch.empty_like(slot_tag)
-    retagged = torch.zeros((), dtype=torch.int64, device="cuda")
-    if ws > 1:
-        import torch.distributed as dist
-        dist.barrier()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    with ClockSampler(local) as clk, torch.cuda.stream(stream):
-        torch.cuda.nvtx.range_push("timed_region")
-        for s in range(steps):
-            if s > 0:
-                prepare(s)
-            if per_token:
-                tag_prev.copy_(slot_tag)
-            l2_flush()
-            step(s, evs[s])
-            counts_acc += cnt_all.sum((0, 1)) if L > 1 else gw.counts.sum(0)
-            if per_token:
-                retagged += (slot_tag != tag_prev).sum()
-        torch.cuda.nvtx.range_pop()
-        torch.cuda.synchronize()
-    wall = time.perf_counter() - t0
-    if ws > 1:
-        dist.barrier()
-    assert gw.pool.get_error() == 0
+    evs, counts_acc, retagged, clk, wall = run_pass(False)
     cnt_sum = counts_acc.cpu().numpy()
-    t_res = [evs[s][0].elapsed_time(evs[s][1]) for s in range(steps)]
-    t_dec = [evs[s][1].elapsed_time(evs[s][2]) for s in range(steps)]
-    ms_step = max_over_ranks((sum(t_res) + sum(t_dec)) / steps)
+    t_step = [evs[s][0].elapsed_time(evs[s][2]) for s in range(steps)]
+    ms_step = max_over_ranks(sum(t_step) / steps)
     steps_per_s = whole_job_rate(1.0, ws, ms_step)
+    evs2, _, _, _, _ = run_pass(True)
+    t_res = [evs2[s][0].elapsed_time(evs2[s][1]) for s in range(steps)]
+    t_dec = [evs2[s][1].elapsed_time(evs2[s][2]) for s in range(steps)]
     res_ms = sum(t_res) / steps
     dec_ms = sum(t_dec) / steps
     rows_per_s = ws * L * w.B * w.K / (res_ms * 1e-3)
@@ -453,6 +476,11 @@ def measure(args, name, steps, with_e2e=False):
         "config": run_config(desc, w, ws, L, args.in_place),
         "resolved_rows_per_s": round(rows_per_s, 1),
         "resolve_ms": round(res_ms, 5), "decode_ms": round(dec_ms, 5),
+        "kernel_times": ("ms_per_step: each timed step from before the resolve to after the "
+                         "decode, nothing between the kernels; resolve_ms and decode_ms: a second "
+                         "pass over the same steps with an event between the kernels, which keeps "
+                         "the decode from launching while the resolve runs (so they add up to "
+                         "more than ms_per_step)"),
         "counts_per_step": {"resident": float(per_step_counts[0]), "hot": float(per_step_counts[1]),
                             "miss": float(per_step_counts[2])},
         **({"per_token": {"entries_per_step": w.B * w.T * w.K, "distinct_rows_per_step": pt[0],
@@ -474,7 +502,7 @@ def measure(args, name, steps, with_e2e=False):
         for t in range(w.turns):
             a, b = t * w.steps_per_turn, min(steps, (t + 1) * w.steps_per_turn)
             if a < b:
-                per_turn.append(round(sum(t_res[a:b]) + sum(t_dec[a:b]), 3))
+                per_turn.append(round(sum(t_step[a:b]), 3))
         line["per_turn_ms"] = per_turn
     if with_e2e and not agent and L == 1:
         line["e2e"] = run_e2e(args, gw, qs, stream, w)
