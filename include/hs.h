@@ -134,6 +134,11 @@ void *hs_gpu_rows(hs_pool_t pool);
 void *hs_host_rows(hs_pool_t pool);
 float *hs_gpu_scales(hs_pool_t pool);  /* NULL for HS_BF16 */
 float *hs_host_scales(hs_pool_t pool); /* NULL for HS_BF16 */
+/* Device addresses of the host arena's mapping (the addresses the resolve
+ * reads misses through), for the caller's own kernels that read the arena.
+ * NULL when the pool has no host arena (scales: also for HS_BF16). */
+void *hs_host_rows_device(hs_pool_t pool);
+float *hs_host_scales_device(hs_pool_t pool);
 
 /* Snapshot / restore of the hot-buffer state of all requests (clock, slot_tag,
  * slot_stamp, lru_order, pos_to_slot) to / from host memory. Synchronous.

@@ -30,7 +30,8 @@ EXPORTED = [
     "hs_pool_create", "hs_pool_destroy", "hs_pool_get_config", "hs_pool_get_tables",
     "hs_request_init", "hs_request_set_ctx_len", "hs_set_ctx_len", "hs_page_map",
     "hs_page_map_range", "hs_hot_lease", "hs_hot_release", "hs_gpu_rows", "hs_host_rows",
-    "hs_gpu_scales", "hs_host_scales", "hs_pool_snapshot", "hs_pool_restore",
+    "hs_gpu_scales", "hs_host_scales", "hs_host_rows_device", "hs_host_scales_device",
+    "hs_pool_snapshot", "hs_pool_restore",
     "hs_pool_get_error", "hs_resolve_topk", "hs_sparse_mla_decode",
     "hs_decode_workspace_bytes", "hs_status_string", "hs_sparse_mla_decode_static_ws",
     "hs_pool_check_bounded_wait", "hs_resolve_topk_union", "hs_sparse_mla_decode_per_token",
@@ -88,6 +89,7 @@ def load() -> C.CDLL:
         "hs_hot_release": ([vp, i32], i32),
         "hs_gpu_rows": ([vp], vp), "hs_host_rows": ([vp], vp),
         "hs_gpu_scales": ([vp], vp), "hs_host_scales": ([vp], vp),
+        "hs_host_rows_device": ([vp], vp), "hs_host_scales_device": ([vp], vp),
         "hs_pool_snapshot": ([vp, vp, sz, C.POINTER(sz)], i32),
         "hs_pool_restore": ([vp, vp, sz], i32),
         "hs_pool_get_error": ([vp, C.POINTER(C.c_uint32)], i32),
@@ -373,6 +375,19 @@ class Pool:
             return None
         n = self.cfg.n_host_blocks * 64
         return np.ctypeslib.as_array((C.c_float * n).from_address(p))
+
+    def host_rows_device(self):
+        """The host arena as seen by the GPU (reads go over the host link), or None."""
+        p = load().hs_host_rows_device(self.handle)
+        if not p:
+            return None
+        return _device_view(p, (self.cfg.n_host_blocks * 64, self.row_bytes), "|u1")
+
+    def host_scales_device(self):
+        p = load().hs_host_scales_device(self.handle)
+        if not p:
+            return None
+        return _device_view(p, (self.cfg.n_host_blocks * 64,), "<f4")
 
     def tables(self) -> dict:
         t, R, C_ = self._tables, self.cfg.max_requests, self.cfg.hot_rows

@@ -310,6 +310,8 @@ void *hs_gpu_rows(hs_pool_t p) { return p ? p->d_rows : nullptr; }
 void *hs_host_rows(hs_pool_t p) { return p ? p->h_rows : nullptr; }
 float *hs_gpu_scales(hs_pool_t p) { return p ? p->d_scales : nullptr; }
 float *hs_host_scales(hs_pool_t p) { return p ? p->h_scales : nullptr; }
+void *hs_host_rows_device(hs_pool_t p) { return p ? p->hd_rows : nullptr; }
+float *hs_host_scales_device(hs_pool_t p) { return p ? p->hd_scales : nullptr; }
 
 hs_status hs_pool_snapshot(hs_pool_t p, void *dst, size_t cap, size_t *used) {
     if (!p) return HS_ERR_INVALID_ARG;
