@@ -208,9 +208,10 @@ DESCS = {
 DEFAULT_STEPS = {"resident": 2000, "tiny": 2000, "hybrid": 512, "noresident": 256, "agent": 715}
 # How each workload's rows reach attention by default: read in place from the
 # pool (no gathered buffer) where that gives the shorter step on a GB300,
-# gathered by the resolve elsewhere (measured: resident 17.6K steps/s in place
-# against 14.0K gathered; the FP8 workloads equal or faster gathered)
-DEFAULT_IN_PLACE = {"resident": True, "tiny": False, "hybrid": False, "noresident": False,
+# gathered by the resolve elsewhere (measured, steps/s in place against
+# gathered: resident 17.7K / 13.6K, tiny 27.4K / 25.7K, hybrid 8.0K / 8.4K,
+# no-resident and agent mix within 1%)
+DEFAULT_IN_PLACE = {"resident": True, "tiny": True, "hybrid": False, "noresident": False,
                     "agent": False}
 
 
