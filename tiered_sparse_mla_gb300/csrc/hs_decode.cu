@@ -1009,12 +1009,41 @@ combine_kernel(const __nv_bfloat16 *__restrict__ ws_o, const float *__restrict__
     const int t = blockIdx.x * 256 + threadIdx.x;
     const int row = t >> 6, c8 = (t & 63) * 8;
     if (row >= rows) return;
-    float mx = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) mx = fmaxf(mx, ws_lse[(size_t)s * rows + row]);
     float acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-    float wsum = 0.f;
+    float wsum = 0.f, mx = -INFINITY;
+    constexpr int MAXS = 4;
+    if (nsplit <= MAXS) {
+        // every load issued before any is used: one memory round trip
+        float ls[MAXS];
+        uint4 u[MAXS];
+#pragma unroll
+        for (int s = 0; s < MAXS; ++s) {
+            ls[s] = -INFINITY;
+            u[s] = make_uint4(0u, 0u, 0u, 0u);
+            if (s < nsplit) {
+                ls[s] = ws_lse[(size_t)s * rows + row];
+                u[s] = *reinterpret_cast<const uint4 *>(ws_o + ((size_t)s * rows + row) * 512 + c8);
+            }
+        }
+#pragma unroll
+        for (int s = 0; s < MAXS; ++s) mx = fmaxf(mx, ls[s]);
+        if (mx != -INFINITY) {
+#pragma unroll
+            for (int s = 0; s < MAXS; ++s) {
+                const float w = ls[s] == -INFINITY ? 0.f : __expf(ls[s] - mx);
+                wsum += w;
+                const uint32_t v[4] = {u[s].x, u[s].y, u[s].z, u[s].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    acc[2 * e] += w * __uint_as_float(v[e] << 16);
+                    acc[2 * e + 1] += w * __uint_as_float(v[e] & 0xffff0000u);
+                }
+            }
+        }
+    } else {
+    for (int s = 0; s < nsplit; ++s) mx = fmaxf(mx, ws_lse[(size_t)s * rows + row]);
     if (mx != -INFINITY) {
 #pragma unroll 4
         for (int s = 0; s < nsplit; ++s) {
@@ -1029,6 +1058,7 @@ combine_kernel(const __nv_bfloat16 *__restrict__ ws_o, const float *__restrict__
                 acc[2 * e + 1] += w * __uint_as_float(v[e] & 0xffff0000u);
             }
         }
+    }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     *reinterpret_cast<uint4 *>(out + (size_t)row * 512 + c8) =
