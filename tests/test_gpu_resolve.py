@@ -286,3 +286,24 @@ def test_layer_group_argument_errors():
         hs.hs_layer_group_create([])
     a.pool.close()
     b.pool.close()
+
+
+def test_host_arena_device_views_read_the_host_bytes():
+    """hs_host_rows_device / hs_host_scales_device: the GPU's view of the pinned
+    host arena (the addresses the resolve reads misses through) holds the same
+    bytes as the CPU's view, read by a GPU kernel."""
+    from harness import GpuWorkload
+    w = W.WORKLOADS["hybrid"].scaled(B=2, ctx=32768, resident_tail=4096, H=16, steps=1)
+    gw = GpuWorkload(w)
+    host = gw.pool.host_rows()
+    dev = gw.pool.host_rows_device()
+    assert host is not None and dev is not None and dev.is_cuda
+    assert tuple(dev.shape) == host.shape
+    rng = np.random.default_rng(5)
+    rows = np.sort(rng.choice(host.shape[0], size=256, replace=False))
+    idx = torch.from_numpy(rows).cuda()
+    got = dev.index_select(0, idx).cpu().numpy()  # a GPU gather over the mapping
+    assert np.array_equal(got, host[rows])
+    hs_, ds_ = gw.pool.host_scales(), gw.pool.host_scales_device()
+    assert np.array_equal(ds_.index_select(0, idx).cpu().numpy(), hs_[rows])
+    gw.pool.close()
