@@ -990,7 +990,10 @@ def main():
     args.steps = args.steps or DEFAULT_STEPS[args.workload]
     if args.in_place and args.gathered:
         ap.error("--in-place and --gathered exclude each other")
-    args.in_place = args.in_place or (not args.gathered and DEFAULT_IN_PLACE[args.workload])
+    # per-token lists (a union resolve): in place measured shorter (hybrid,
+    # 5.6K against 5.0K steps/s), whatever the workload's default
+    args.in_place = args.in_place or (not args.gathered and
+                                      (DEFAULT_IN_PLACE[args.workload] or args.per_token))
     if args.impl == "reference":
         run_reference(args)
     elif args.transitions:
