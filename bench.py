@@ -991,7 +991,7 @@ def main():
     if args.in_place and args.gathered:
         ap.error("--in-place and --gathered exclude each other")
     # per-token lists (a union resolve): in place measured shorter (hybrid,
-    # 5.6K against 5.0K steps/s), whatever the workload's default
+    # 5.9K against 5.3K steps/s), whatever the workload's default
     args.in_place = args.in_place or (not args.gathered and
                                       (DEFAULT_IN_PLACE[args.workload] or args.per_token))
     if args.impl == "reference":
