@@ -77,6 +77,10 @@ SMALL = {
                                                     hot_rows=2048, tail=100, H=24, T=3,
                                                     steps=2), 2),
     "noresident": (W.WORKLOADS["noresident"].scaled(B=3, ctx=32768, H=16, steps=2), 2),
+    # BF16 rows, K = 1000: eight splits of 128 keys, the last one's second tile
+    # holds 40 keys (keys 32-39 valid in the half the second copying warp takes)
+    "resident_ragged": (W.WORKLOADS["resident"].scaled(B=2, ctx=16384, H=64, K=1000, tail=100,
+                                                       steps=2), 2),
 }
 
 
@@ -130,7 +134,7 @@ def test_decode_in_place_edge_cases():
     _decode_case(w, 1, topk_override=lists, in_place=True)
 
 
-@pytest.mark.parametrize("name", ["resident", "hybrid_ragged", "noresident"])
+@pytest.mark.parametrize("name", ["resident", "resident_ragged", "hybrid_ragged", "noresident"])
 def test_decode_in_place_matches_gathered_bitwise(name):
     """The same rows reach the same tiles either way, so the outputs are identical."""
     from harness import GpuWorkload
