@@ -273,10 +273,13 @@ __device__ __forceinline__ void resolve_body(PT P, const int32_t *__restrict__ r
     const int tid = threadIdx.x;
     const int g = static_cast<int>(hs::cluster_ctarank());
     const int bi = blockIdx.y;
-    const int r = req_ids[bi];
     const int j0 = (g - 1) * chunk;  // first list entry of a worker
     const int nloc = g == 0 ? 0 : max(0, min(K, j0 + chunk) - j0);
     const size_t row0 = (size_t)bi * K + (g == 0 ? 0 : j0);  // first gathered row of this CTA
+    // a worker's first list entry is loaded before anything else: its latency
+    // overlaps the request's loads and the cluster barrier below
+    const int p_first = tid < nloc ? topk[row0 + tid] : -1;
+    const int r = req_ids[bi];
     const bool fp8 = P.scales != nullptr;
     const bool gath = gathered != nullptr;  // else rows are read in place by attention
 
@@ -322,7 +325,7 @@ __device__ __forceinline__ void resolve_body(PT P, const int32_t *__restrict__ r
         int n_res = 0, n_hot = 0;
         for (int lb = 0; lb < nloc; lb += NT) {  // warp-uniform trip count
             const int l = lb + tid;
-            const int p = l < nloc ? topk[row0 + l] : -1;
+            const int p = lb == 0 ? p_first : (l < nloc ? topk[row0 + l] : -1);
             int kind = KIND_NONE, src = -1, hrow = -1;
             if (l >= nloc || p == -1) {
             } else if (p < 0 || p >= Lr || p >= P.max_ctx) {
