@@ -306,12 +306,19 @@ __device__ __forceinline__ void resolve_body(PT P, const int32_t *__restrict__ r
     int32_t *stamp = P.stamp + (size_t)r * C;
     int32_t *lru = P.lru + (size_t)r * C;
     int32_t *p2s = P.p2s + (size_t)r * P.max_ctx;
+    // the first entry's page-table entry, also before the barrier
+    const int2 e_first = (p_first >= 0 && p_first < P.max_ctx) ? page[p_first >> 6] : make_int2(-1, -1);
 
     if (tid == 0) s_misc[0] = s_misc[1] = s_misc[2] = s_misc[3] = s_misc[4] = 0;
     // every CTA of the cluster is running (and has set up its shared memory)
-    // before any distributed-shared-memory store below
+    // before any distributed-shared-memory store below; rank 0 releases its
+    // counters, a worker publishes nothing here, so its arrive does not wait
+    // for the loads above
     __syncthreads();
-    hs::cluster_arrive();
+    if (g == 0)
+        hs::cluster_arrive();
+    else
+        asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
     hs::cluster_wait();
 
     uint32_t err = 0;
@@ -331,7 +338,7 @@ __device__ __forceinline__ void resolve_body(PT P, const int32_t *__restrict__ r
             } else if (p < 0 || p >= Lr || p >= P.max_ctx) {
                 err |= HS_DEVERR_INDEX_RANGE;
             } else {
-                const int2 e = page[p >> 6];
+                const int2 e = lb == 0 ? e_first : page[p >> 6];
                 if (e.x >= 0) {
                     kind = KIND_RES;
                     src = e.x * hs::kPage + (p & 63);
