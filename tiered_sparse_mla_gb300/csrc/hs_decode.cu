@@ -999,72 +999,93 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 }
 
 // Merges the KV-split partials: out = sum_s w_s O_s / sum_s w_s, w_s = exp(lse_s - max).
-// One thread per 8 output columns of a row (64 threads per row): every load
-// of a thread is independent of the others, so the whole merge is about one
-// round trip to memory.
-__global__ void __launch_bounds__(256)
-combine_kernel(const __nv_bfloat16 *__restrict__ ws_o, const float *__restrict__ ws_lse, int nsplit,
-               int rows, __nv_bfloat16 *__restrict__ out, float *__restrict__ lse) {
-    grid_dep_wait();  // the decode grid's partials are complete
-    const int t = blockIdx.x * 256 + threadIdx.x;
-    const int row = t >> 6, c8 = (t & 63) * 8;
-    if (row >= rows) return;
-    float acc[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-    float wsum = 0.f, mx = -INFINITY;
-    constexpr int MAXS = 4;
-    if (nsplit <= MAXS) {
-        // every load issued before any is used: one memory round trip
-        float ls[MAXS];
-        uint4 u[MAXS];
-#pragma unroll
-        for (int s = 0; s < MAXS; ++s) {
-            ls[s] = -INFINITY;
-            u[s] = make_uint4(0u, 0u, 0u, 0u);
-            if (s < nsplit) {
-                ls[s] = ws_lse[(size_t)s * rows + row];
-                u[s] = *reinterpret_cast<const uint4 *>(ws_o + ((size_t)s * rows + row) * 512 + c8);
-            }
-        }
-#pragma unroll
-        for (int s = 0; s < MAXS; ++s) mx = fmaxf(mx, ls[s]);
-        if (mx != -INFINITY) {
-#pragma unroll
-            for (int s = 0; s < MAXS; ++s) {
-                const float w = ls[s] == -INFINITY ? 0.f : __expf(ls[s] - mx);
-                wsum += w;
-                const uint32_t v[4] = {u[s].x, u[s].y, u[s].z, u[s].w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    acc[2 * e] += w * __uint_as_float(v[e] << 16);
-                    acc[2 * e + 1] += w * __uint_as_float(v[e] & 0xffff0000u);
-                }
-            }
-        }
-    } else {
-    for (int s = 0; s < nsplit; ++s) mx = fmaxf(mx, ws_lse[(size_t)s * rows + row]);
-    if (mx != -INFINITY) {
-#pragma unroll 4
-        for (int s = 0; s < nsplit; ++s) {
-            const float ls = ws_lse[(size_t)s * rows + row];
-            const uint4 u = *reinterpret_cast<const uint4 *>(ws_o + ((size_t)s * rows + row) * 512 + c8);
-            const float w = ls == -INFINITY ? 0.f : __expf(ls - mx);
-            wsum += w;
-            const uint32_t v[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                acc[2 * e] += w * __uint_as_float(v[e] << 16);
-                acc[2 * e + 1] += w * __uint_as_float(v[e] & 0xffff0000u);
-            }
-        }
-    }
-    }
+// One task per 8 output columns of a row (64 tasks per row), two tasks per
+// thread a grid apart: every load of both is issued before any is used, so the
+// whole merge is about one round trip to memory, with half as many blocks to
+// place once the decode's CTAs leave their SMs.
+constexpr int CMB_TPT = 2;
+__device__ __forceinline__ void combine_store(__nv_bfloat16 *__restrict__ out, float *__restrict__ lse,
+                                              int row, int c8, const float (&acc)[8], float wsum, float mx) {
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     *reinterpret_cast<uint4 *>(out + (size_t)row * 512 + c8) =
         make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
                    pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
     if (c8 == 0) lse[row] = wsum > 0.f ? mx + __logf(wsum) : -INFINITY;
+}
+__global__ void __launch_bounds__(256)
+combine_kernel(const __nv_bfloat16 *__restrict__ ws_o, const float *__restrict__ ws_lse, int nsplit,
+               int rows, __nv_bfloat16 *__restrict__ out, float *__restrict__ lse) {
+    grid_dep_wait();  // the decode grid's partials are complete
+    const int t0 = blockIdx.x * 256 + threadIdx.x, stride = gridDim.x * 256;
+    constexpr int MAXS = 4;
+    if (nsplit <= MAXS) {
+        float ls[CMB_TPT][MAXS];
+        uint4 u[CMB_TPT][MAXS];
+#pragma unroll
+        for (int q = 0; q < CMB_TPT; ++q) {
+            const int t = t0 + q * stride, row = t >> 6, c8 = (t & 63) * 8;
+#pragma unroll
+            for (int s = 0; s < MAXS; ++s) {
+                ls[q][s] = -INFINITY;
+                u[q][s] = make_uint4(0u, 0u, 0u, 0u);
+                if (row < rows && s < nsplit) {
+                    ls[q][s] = ws_lse[(size_t)s * rows + row];
+                    u[q][s] = *reinterpret_cast<const uint4 *>(ws_o + ((size_t)s * rows + row) * 512 + c8);
+                }
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < CMB_TPT; ++q) {
+            const int t = t0 + q * stride, row = t >> 6, c8 = (t & 63) * 8;
+            if (row >= rows) continue;
+            float acc[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+            float wsum = 0.f, mx = -INFINITY;
+#pragma unroll
+            for (int s = 0; s < MAXS; ++s) mx = fmaxf(mx, ls[q][s]);
+            if (mx != -INFINITY) {
+#pragma unroll
+                for (int s = 0; s < MAXS; ++s) {
+                    const float w = ls[q][s] == -INFINITY ? 0.f : __expf(ls[q][s] - mx);
+                    wsum += w;
+                    const uint32_t v[4] = {u[q][s].x, u[q][s].y, u[q][s].z, u[q][s].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        acc[2 * e] += w * __uint_as_float(v[e] << 16);
+                        acc[2 * e + 1] += w * __uint_as_float(v[e] & 0xffff0000u);
+                    }
+                }
+            }
+            combine_store(out, lse, row, c8, acc, wsum, mx);
+        }
+    } else {
+        for (int q = 0; q < CMB_TPT; ++q) {
+            const int t = t0 + q * stride, row = t >> 6, c8 = (t & 63) * 8;
+            if (row >= rows) continue;
+            float acc[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+            float wsum = 0.f, mx = -INFINITY;
+            for (int s = 0; s < nsplit; ++s) mx = fmaxf(mx, ws_lse[(size_t)s * rows + row]);
+            if (mx != -INFINITY) {
+#pragma unroll 4
+                for (int s = 0; s < nsplit; ++s) {
+                    const float l = ws_lse[(size_t)s * rows + row];
+                    const uint4 v4 = *reinterpret_cast<const uint4 *>(ws_o + ((size_t)s * rows + row) * 512 + c8);
+                    const float w = l == -INFINITY ? 0.f : __expf(l - mx);
+                    wsum += w;
+                    const uint32_t v[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        acc[2 * e] += w * __uint_as_float(v[e] << 16);
+                        acc[2 * e + 1] += w * __uint_as_float(v[e] & 0xffff0000u);
+                    }
+                }
+            }
+            combine_store(out, lse, row, c8, acc, wsum, mx);
+        }
+    }
 }
 
 // ---------------------------------------------------------------- host side
@@ -1289,7 +1310,7 @@ hs_status decode_entry(hs_pool_t pool, int32_t B, int32_t T, int32_t tpl, int32_
     if (pl.nsplit > 1) {
         const int rows = B * pl.M;
         cudaLaunchConfig_t cc = {};
-        cc.gridDim = dim3((rows + 3) / 4, 1, 1);
+        cc.gridDim = dim3((rows + 4 * CMB_TPT - 1) / (4 * CMB_TPT), 1, 1);  // 4 rows per block and task
         cc.blockDim = dim3(256, 1, 1);
         cc.stream = s;
         cudaLaunchAttribute ca[1];
