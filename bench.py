@@ -667,22 +667,27 @@ def run_e2e(args, gw, qs, stream, w):
     """Same step through the C ABI, inputs copied from pinned host memory and the
     result (out, lse) read back to host memory inside the timed region.
 
-    The copies run on two more streams (uploads and downloads, which the host
-    link carries in both directions at once), double-buffered, the way a
-    serving loop overlaps them: step s+1's top-K lists and q go up while step s
-    computes, and step s's out and lse come back while step s+1 computes. Every
-    step still moves its own inputs and result; the timed region ends when the
-    last result is in host memory.
-
-    The step's two calls (resolve, decode) are captured once per buffer in a
-    CUDA graph (the calls are capturable: the launch shapes depend only on the
-    sizes, and the LRU clock advances in device memory) and replayed, so the
-    host issues one launch per step instead of two library calls."""
+    Each step is one CUDA-graph launch with three branches: the step's two
+    library calls (resolve, decode) on its input buffer; the upload of the
+    next step's top-K lists and q from pinned host memory into the other
+    buffer; and the download of the previous step's out and lse from that
+    buffer into pinned host memory. The copies overlap the compute in both
+    directions, every step still moves its own inputs and result, and the host
+    issues one launch per step: issued from Python one by one, the four copies,
+    the two calls and the events that order them cost about as much host time
+    as the GPU spends on the step, and the loop ran at the host's pace. The
+    graphs are captured once per position in the cycle of inputs (each names
+    its buffers and pinned host arrays) and replayed; the calls are capturable
+    (the launch shapes depend only on the sizes, and the LRU clock advances in
+    device memory). The timed region starts before the first step's upload and
+    ends when the last step's result is in host memory."""
+    import math
     import torch
     # a fixed count, whatever the timed region's: with a few steps the first
     # ones (launch pipeline filling, copy engines starting) dominate
     n = 200
-    topk_h = [gw.topk[s % w.steps].cpu().pin_memory() for s in range(w.steps)]
+    nt, nq = w.steps, len(qs)
+    topk_h = [gw.topk[s].cpu().pin_memory() for s in range(nt)]
     q_h = [q.cpu().pin_memory() for q in qs]
     out_h = [torch.empty(gw.out.shape, dtype=gw.out.dtype).pin_memory() for _ in range(2)]
     lse_h = [torch.empty(gw.lse.shape, dtype=gw.lse.dtype).pin_memory() for _ in range(2)]
@@ -692,81 +697,59 @@ def run_e2e(args, gw, qs, stream, w):
     lse_d = [torch.empty_like(gw.lse) for _ in range(2)]
     h2d = topk_h[0].numel() * 4 + q_h[0].numel() * 2
     d2h = out_h[0].numel() * 2 + lse_h[0].numel() * 4
-    cp = torch.cuda.Stream()   # uploads
-    cpd = torch.cuda.Stream()  # downloads
-    ev = lambda: torch.cuda.Event()
-    # one graph per buffer: resolve the lists in t_d[i], attend with q_d[i]
-    # into out_d[i], lse_d[i] (capture records the launches, runs nothing)
+    cycle = math.lcm(nt, nq, 2)
+    up_s, dn_s, cap = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     graphs = []
-    cap = torch.cuda.Stream()
-    for i in range(2):
+    for s in range(cycle):
+        i, j = s % 2, (s + 1) % 2  # this step's buffer; the next step's and the previous one's
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=cap):
-            cs = torch.cuda.current_stream()
+            main = torch.cuda.current_stream()
+            up_s.wait_stream(main)
+            dn_s.wait_stream(main)
+            with torch.cuda.stream(up_s):
+                t_d[j].copy_(topk_h[(s + 1) % nt], non_blocking=True)
+                q_d[j].copy_(q_h[(s + 1) % nq], non_blocking=True)
+            with torch.cuda.stream(dn_s):
+                out_h[j].copy_(out_d[j], non_blocking=True)
+                lse_h[j].copy_(lse_d[j], non_blocking=True)
             gw.pool.resolve_topk(gw.req_ids, t_d[i], gw.resolved, gw.gathered, gw.gscale,
-                                 gw.counts, cs)
+                                 gw.counts, main)
             gw.pool.sparse_mla_decode(q_d[i], gw.gathered, gw.gscale, gw.resolved, t_d[i],
                                       gw.req_ids, w.sm_scale, out_d[i], lse_d[i], gw.workspace,
-                                      cs)
+                                      main)
+            main.wait_stream(up_s)
+            main.wait_stream(dn_s)
         graphs.append(g)
     torch.cuda.synchronize()
 
     def run(nsteps):
-        up = [None, None]        # inputs of buffer i are on the device
-        done = [None, None]      # step using buffer i has finished computing
-        down = [None, None]      # result of buffer i is in host memory
-
-        def upload(s):
-            i = s % 2
-            with torch.cuda.stream(cp):
-                if done[i] is not None:
-                    cp.wait_event(done[i])  # step s-2 no longer reads buffer i
-                t_d[i].copy_(topk_h[s % w.steps], non_blocking=True)
-                q_d[i].copy_(q_h[s % len(q_h)], non_blocking=True)
-                up[i] = ev()
-                up[i].record(cp)
-
-        upload(0)
+        # the first step's inputs, one launch per step, the last step's result
+        t_d[0].copy_(topk_h[0], non_blocking=True)
+        q_d[0].copy_(q_h[0], non_blocking=True)
         for s in range(nsteps):
-            i = s % 2
-            if s + 1 < nsteps:
-                upload(s + 1)
-            stream.wait_event(up[i])
-            if down[i] is not None:
-                stream.wait_event(down[i])  # step s-2's result has left buffer i
-            with torch.cuda.stream(stream):
-                graphs[i].replay()
-            done[i] = ev()
-            done[i].record(stream)
-            with torch.cuda.stream(cpd):
-                cpd.wait_event(done[i])
-                out_h[i].copy_(out_d[i], non_blocking=True)
-                lse_h[i].copy_(lse_d[i], non_blocking=True)
-                down[i] = ev()
-                down[i].record(cpd)
-        for d in down:
-            if d is not None:
-                stream.wait_event(d)
+            graphs[s % cycle].replay()
+        k = (nsteps - 1) % 2
+        out_h[k].copy_(out_d[k], non_blocking=True)
+        lse_h[k].copy_(lse_d[k], non_blocking=True)
 
-    run(10)
+    with torch.cuda.stream(stream):
+        run(10)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    cp.wait_stream(stream)
-    cpd.wait_stream(stream)
-    e0.record(stream)
-    cp.wait_event(e0)
-    cpd.wait_event(e0)
-    run(n)
-    e1.record(stream)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        run(n)
+        e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / n
     ws, _, _ = _dist()
     return {"value": round(ws / (ms * 1e-3), 2), "unit": "decode steps/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
-            "note": ("pinned host inputs (top-K lists, q) and outputs (out, lse), uploads and "
-                     "downloads each on their own stream with double buffers, overlapping the "
-                     "neighbouring steps' compute; the step's resolve and decode calls captured "
-                     "once per buffer in a CUDA graph and replayed; L2 not flushed")}
+            "note": ("pinned host inputs (top-K lists, q) and outputs (out, lse); each step one "
+                     "CUDA-graph launch holding the step's resolve and decode calls, the upload "
+                     "of the next step's inputs and the download of the previous step's result "
+                     "as parallel branches (double buffers); L2 not flushed")}
 
 
 # ------------------------------------------------------------------ CPU oracle
