@@ -663,7 +663,7 @@ def run_transitions(args):
     pool.close()
 
 
-def run_e2e(args, gw, qs, stream, w):
+def run_e2e(args, gw, qs, stream, w, check=False):
     """Same step through the C ABI, inputs copied from pinned host memory and the
     result (out, lse) read back to host memory inside the timed region.
 
@@ -680,7 +680,10 @@ def run_e2e(args, gw, qs, stream, w):
     its buffers and pinned host arrays) and replayed; the calls are capturable
     (the launch shapes depend only on the sizes, and the LRU clock advances in
     device memory). The timed region starts before the first step's upload and
-    ends when the last step's result is in host memory."""
+    ends when the last step's result is in host memory. check: afterwards, the
+    last step's downloaded out and lse are compared bit for bit with eager
+    calls on that step's inputs (a resident workload, whose LRU state does not
+    change between steps), and the result is added as "check"."""
     import math
     import torch
     # a fixed count, whatever the timed region's: with a few steps the first
@@ -744,7 +747,20 @@ def run_e2e(args, gw, qs, stream, w):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / n
     ws, _, _ = _dist()
-    return {"value": round(ws / (ms * 1e-3), 2), "unit": "decode steps/s",
+    extra = {}
+    if check:
+        last, k = n - 1, (n - 1) % 2
+        with torch.cuda.stream(stream):
+            t_e, q_e = topk_h[last % nt].cuda(), q_h[last % nq].cuda()
+            gw.pool.resolve_topk(gw.req_ids, t_e, gw.resolved, gw.gathered, gw.gscale, gw.counts,
+                                 stream)
+            gw.pool.sparse_mla_decode(q_e, gw.gathered, gw.gscale, gw.resolved, t_e, gw.req_ids,
+                                      w.sm_scale, gw.out, gw.lse, gw.workspace, stream)
+        torch.cuda.synchronize()
+        extra["check"] = {
+            "out_equal": bool(torch.equal(out_h[k].view(torch.int16), gw.out.cpu().view(torch.int16))),
+            "lse_equal": bool(torch.equal(lse_h[k].view(torch.int32), gw.lse.cpu().view(torch.int32)))}
+    return {**extra, "value": round(ws / (ms * 1e-3), 2), "unit": "decode steps/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
             "note": ("pinned host inputs (top-K lists, q) and outputs (out, lse); each step one "
                      "CUDA-graph launch holding the step's resolve and decode calls, the upload "

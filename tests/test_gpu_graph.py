@@ -63,3 +63,23 @@ def test_graph_replay_matches_eager():
     assert torch.equal(gw.pool.tables()["clock"], clock0 + w.steps)
     assert gw.pool.get_error() == 0
     gw.pool.close()
+
+
+def test_bench_e2e_pipeline_results():
+    """The bench's end-to-end loop (one graph launch per step: the step's calls,
+    the next step's upload and the previous step's download as parallel
+    branches) hands back, in pinned host memory, exactly what eager calls on
+    the same inputs give."""
+    import bench
+    from harness import GpuWorkload
+    w = W.WORKLOADS["resident"].scaled(B=4, ctx=16384, steps=6)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        gw = GpuWorkload(w, stream=stream, in_place=True)
+        qs = [W.make_q(w, s, device="cuda") for s in range(4)]
+    torch.cuda.synchronize()
+    r = bench.run_e2e(None, gw, qs, stream, w, check=True)
+    assert r["check"] == {"out_equal": True, "lse_equal": True}, r["check"]
+    assert r["h2d_bytes_per_step"] == w.B * w.K * 4 + w.B * w.T * w.H * 576 * 2
+    assert r["d2h_bytes_per_step"] == w.B * w.T * w.H * (512 * 2 + 4)
+    gw.pool.close()
