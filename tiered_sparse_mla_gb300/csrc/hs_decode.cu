@@ -54,11 +54,12 @@
 //   warps 4-7   stagers, one thread per query row (TMEM lane): read S_j, free
 //               it for the next QK, scale it and write both halves to the
 //               outgoing buffers; FP8: also convert each landed tile of codes
-//               to BF16 in place, two tiles ahead of its QK;
+//               to BF16 in place, two tiles ahead of its QK; BF16: output
+//               columns 128-255 of the epilogue;
 //   warps 8-11  softmax, one thread per query row, per half tile: add the two
 //               partials, mask, online softmax with a conditional rescale, P
 //               to TMEM; then the epilogue (O / l through shared memory and
-//               TMA stores).
+//               TMA stores; BF16 rows: columns 0-127).
 // TMEM (512 columns): O half 256 | S 64 | P 32 | Q 144.
 // Every mbarrier wait is bounded in time; on expiry the kernel sets
 // HS_DEVERR_TIMEOUT, drains its own copies and MMAs and returns. Roles hand
@@ -703,6 +704,49 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         tc_fence_before();
         mbar_arrive(bar(C::B_QREADY));
 
+        // Epilogue: O / l as BF16 through shared memory (the ring is idle once
+        // the last PV is done): 32-column TMEM loads into 64-column boxes of
+        // the 128-byte-swizzled layout, then one TMA store per box (rows past
+        // M are clipped by the tensor map). BF16 rows: the softmax warp of a
+        // lane quarter writes columns 0-127 of its 32 rows and the stager warp
+        // of the same quarter, idle by then, columns 128-255; the softmax warp
+        // hands 1/l (-1 after a failed wait) to it through shared memory and a
+        // named barrier of the two warps. FP8 rows: the stagers may still be
+        // converting codes, so the softmax warp writes all 256 columns.
+        float *s_inv = reinterpret_cast<float *>(smem + C::OFF_RING + 65536);  // [BM], past the staging
+        auto store_o = [&](int cc0, int ncc, float inv) {
+            const uint32_t stg = sR + (uint32_t)wq * 16384u;
+#pragma unroll 1
+            for (int cc = cc0; cc < cc0 + ncc; ++cc) {
+                uint32_t o[32];
+                HS_TMEM_LD32(tmem + lane_off + TM_O + 32 * cc, o);
+                HS_TMEM_WAIT_LD32(o);
+                const uint32_t box = stg + (uint32_t)(cc >> 1) * 4096u + (uint32_t)lane * 128u;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        w[e] = pack_bf16(__uint_as_float(o[8 * q + 2 * e]) * inv,
+                                         __uint_as_float(o[8 * q + 2 * e + 1]) * inv);
+                    const int c = (cc & 1) * 4 + q;
+                    st_shared_v4(box + (uint32_t)((c ^ (lane & 7)) << 4), w[0], w[1], w[2], w[3]);
+                }
+            }
+            fence_proxy_async();  // the TMA stores read what the threads wrote
+            __syncwarp();
+            if (lane == 0) {
+                const int zb = p.nsplit == 1 ? b : split * p.B + b;
+                for (int cg = cc0 >> 1; cg < (cc0 + ncc) >> 1; ++cg)
+                    tma_store_3d(&tm_o, stg + (uint32_t)cg * 4096u, half * 256 + cg * 64,
+                                 mt * BM + wq * 32, zb);
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                // the stores have read shared memory before the CTA may exit
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            }
+            __syncwarp();
+        };
+
         if (stager) {
             // ------------------------------------------------ stagers (FP8: and converters)
             // FP8, tile i: read every code of the group (20 KB, ten 16-byte
@@ -808,6 +852,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     mbar_arrive(bar(C::B_STAGED + x));
                 }
                 if (FP8 && j + 2 < ntiles) convert(j + 2);
+            }
+            if (!FP8) {
+                named_bar_sync(4 + wq, 64);  // 1/l of this quarter's rows from its softmax warp
+                const float inv = s_inv[row];
+                if (inv >= 0.f) {
+                    tc_fence_after();
+                    store_o(4, 4, inv);
+                }
             }
         } else {
             // ------------------------------------------------ softmax, PV, epilogue
@@ -945,42 +997,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             if (!ok) fail();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const size_t orow = (size_t)b * p.M + mg;
-            if (ok) {
-                // O / l as BF16 through shared memory (the ring is idle once the
-                // last PV is done): this warp's 32 rows x 256 columns as four
-                // 64-column boxes in the 128-byte-swizzled layout, then four
-                // TMA stores (rows past M are clipped by the tensor map)
-                const uint32_t stg = sR + (uint32_t)wq * 16384u;
-#pragma unroll 1
-                for (int cc = 0; cc < 8; ++cc) {
-                    uint32_t o[32];
-                    HS_TMEM_LD32(tmem + lane_off + TM_O + 32 * cc, o);
-                    HS_TMEM_WAIT_LD32(o);
-                    const uint32_t box = stg + (uint32_t)(cc >> 1) * 4096u + (uint32_t)lane * 128u;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            w[e] = pack_bf16(__uint_as_float(o[8 * q + 2 * e]) * inv,
-                                             __uint_as_float(o[8 * q + 2 * e + 1]) * inv);
-                        const int c = (cc & 1) * 4 + q;
-                        st_shared_v4(box + (uint32_t)((c ^ (lane & 7)) << 4), w[0], w[1], w[2], w[3]);
-                    }
-                }
-                fence_proxy_async();  // the TMA stores read what the threads wrote
-                __syncwarp();
-                if (lane == 0) {
-                    const int zb = p.nsplit == 1 ? b : split * p.B + b;
-                    for (int cg = 0; cg < 4; ++cg)
-                        tma_store_3d(&tm_o, stg + (uint32_t)cg * 4096u, half * 256 + cg * 64,
-                                     mt * BM + wq * 32, zb);
-                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-                    // the stores have read shared memory before the CTA may exit
-                    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-                }
-                __syncwarp();
+            if (!FP8) {
+                s_inv[row] = ok ? inv : -1.f;
+                named_bar_sync(4 + wq, 64);
             }
+            if (ok) store_o(0, FP8 ? 8 : 4, inv);
             if (vrow && half == 0) {
                 const float lse = (ok && l > 0.f) ? (m2 + __log2f(l)) * 0.69314718055994531f : -INFINITY;
                 if (p.nsplit == 1)
