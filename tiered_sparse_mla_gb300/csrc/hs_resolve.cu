@@ -85,8 +85,10 @@ struct Smem {
     __host__ __device__ size_t off_victim() const { return off_keys() + 8 * (size_t)kpad; }
     __host__ __device__ size_t off_lru() const { return off_victim() + 4 * (size_t)(K < C ? K : C); }
     __host__ __device__ size_t off_prot() const { return off_lru() + 4 * (size_t)C; }
+    // rank 0: the counts of block_rank8
+    __host__ __device__ size_t off_rank() const { return (off_prot() + (size_t)C + 15) & ~size_t(15); }
     __host__ __device__ size_t total() const {
-        const size_t r0 = off_prot() + (size_t)C;
+        const size_t r0 = off_rank() + 4 * (size_t)(8 * NT / 32 + 1);
         return r0 > off_stage() ? r0 : off_stage();
     }
 };
@@ -95,6 +97,49 @@ __host__ __device__ inline int next_pow2(int x) {
     int p = 1;
     while (p < x) p <<= 1;
     return p;
+}
+
+// Ranks, in block order, of up to 8 * NT flags: flag (it, t) stands for
+// element it * NT + t, and rank[it] counts the set flags before it. Each warp
+// ballots its 8 rows of flags, one warp scans the 8 * NT / 32 counts (four per
+// lane), so 8 * NT elements take two __syncthreads instead of one block-wide
+// scan per NT. Returns the number of set flags; s_cnt holds 8 * NT / 32 + 1
+// ints and may be reused after the caller's next __syncthreads.
+__device__ __forceinline__ int block_rank8(const bool (&f)[8], int (&rank)[8], int *s_cnt, int tid) {
+    constexpr int NW = NT / 32;
+    static_assert(8 * NW == 4 * 32, "one warp scans the counts, four per lane");
+    const int lane = tid & 31, w = tid >> 5;
+    unsigned bal[8];
+#pragma unroll
+    for (int it = 0; it < 8; ++it) bal[it] = __ballot_sync(0xffffffffu, f[it]);
+    if (lane == 0)
+#pragma unroll
+        for (int it = 0; it < 8; ++it) s_cnt[it * NW + w] = __popc(bal[it]);
+    __syncthreads();
+    if (w == 0) {
+        int v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = s_cnt[4 * lane + e];
+        const int t4 = (v[0] + v[1]) + (v[2] + v[3]);
+        int incl = t4;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        int run = incl - t4;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            s_cnt[4 * lane + e] = run;
+            run += v[e];
+        }
+        if (lane == 31) s_cnt[8 * NW] = incl;
+    }
+    __syncthreads();
+    const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) rank[it] = s_cnt[it * NW + w] + __popc(bal[it] & lt);
+    return s_cnt[8 * NW];
 }
 
 __device__ __forceinline__ void dsmem_st64(uint32_t a, unsigned long long v) {
@@ -265,6 +310,7 @@ __device__ __forceinline__ void resolve_body(PT P, const int32_t *__restrict__ r
     int32_t *s_victim = reinterpret_cast<int32_t *>(smem + L.off_victim());
     int32_t *s_lru = reinterpret_cast<int32_t *>(smem + L.off_lru());
     uint8_t *s_prot = smem + L.off_prot();
+    int32_t *s_rank = reinterpret_cast<int32_t *>(smem + L.off_rank());
     // workers: the end of their shared memory stages the miss rows they read
     // from the host (rows beyond its capacity are read directly)
     uint8_t *s_stage = smem + L.off_stage();
@@ -651,26 +697,30 @@ __device__ __forceinline__ void resolve_body(PT P, const int32_t *__restrict__ r
             // the remaining unprotected slots move to the front
             int nu = 0;
             const int mv = leased ? m : 0;
-            for (int base = 0; base < C; base += NT) {
-                const int i = base + tid;
-                int o = -1, u = 0;
-                if (i < C) {
-                    const int v = s_lru[i];
-                    o = v & 0x7fffffff;
-                    u = v < 0;
+            for (int c0 = 0; c0 < C; c0 += 8 * NT) {
+                bool u[8];
+                int o[8], rk[8];
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    const int i = c0 + it * NT + tid;
+                    const int v = i < C ? s_lru[i] : 0;
+                    o[it] = v & 0x7fffffff;
+                    u[it] = v < 0;
                 }
-                int tot;
-                const int pre = hs::block_scan_flag<NT>(u, s_warp, tot);
-                if (u) {
-                    const int k = nu + pre;
+                const int tot = block_rank8(u, rk, s_rank, tid);
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    if (!u[it]) continue;
+                    const int k = nu + rk[it];
                     if (k < mv) {
-                        s_victim[k] = o;
-                        s_prot[o] = 1;  // stamped this step once placed
+                        s_victim[k] = o[it];
+                        s_prot[o[it]] = 1;  // stamped this step once placed
                     } else {
-                        lru[k - mv] = o;
+                        lru[k - mv] = o[it];
                     }
                 }
                 nu += tot;
+                __syncthreads();  // s_rank is reused
             }
             const int mvict = min(mv, nu);
             __syncthreads();
@@ -711,13 +761,20 @@ __device__ __forceinline__ void resolve_body(PT P, const int32_t *__restrict__ r
             __syncthreads();
             // the slots stamped this step, in slot order, close the LRU order
             int out = nu - mvict;
-            for (int base = 0; base < C; base += NT) {
-                const int s = base + tid;
-                const int f = (s < C) && s_prot[s];
-                int tot;
-                const int pre = hs::block_scan_flag<NT>(f, s_warp, tot);
-                if (f) lru[out + pre] = s;
+            for (int c0 = 0; c0 < C; c0 += 8 * NT) {
+                bool f[8];
+                int rk[8];
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    const int sl = c0 + it * NT + tid;
+                    f[it] = sl < C && s_prot[sl];
+                }
+                const int tot = block_rank8(f, rk, s_rank, tid);
+#pragma unroll
+                for (int it = 0; it < 8; ++it)
+                    if (f[it]) lru[out + rk[it]] = c0 + it * NT + tid;
                 out += tot;
+                __syncthreads();  // s_rank is reused
             }
             served = s_misc[3];  // misses resolved, counting the repeats of a union
         }
