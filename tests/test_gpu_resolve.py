@@ -52,6 +52,9 @@ SMALL = {
     # more miss rows per CTA than its shared memory stages: the rest are read
     # from the host directly
     "noresident_bf16": W.WORKLOADS["noresident"].scaled(B=2, ctx=32768, dtype="bf16", steps=3),
+    # a hot buffer of 8,192 slots: rank 0 ranks its LRU order in two chunks of
+    # 4,096 (eight rows of 512 flags each)
+    "noresident_big_hot": W.WORKLOADS["noresident"].scaled(B=2, ctx=65536, hot_rows=8192, steps=5),
 }
 
 
